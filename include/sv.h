@@ -1,0 +1,228 @@
+/*
+ * sv.h -- C ABI of libsv, the GB300 (sm_103a) SparseVILA hot path.
+ *
+ * The operations follow "SparseVILA: Decoupling Visual Sparsity for Efficient
+ * VLM Inference" (arXiv 2510.17777) as summarised on velog.io (§2 table, §3.1
+ * Prefill Phase, §3.2 Decode Phase, §4.1 Setup) and reviewed on xllm-io
+ * (§三 core formulas, §五 code analysis):
+ *   prefill  -- query-agnostic salience from the encoder's self-attention,
+ *               top-k prune and compaction of the kept tokens;
+ *   decode   -- query-aware retrieval of the most relevant cached visual
+ *               tokens and attention over them plus all text tokens;
+ *   rounds   -- partial eviction of the previous question/answer KV.
+ *
+ * General conventions (every call):
+ *   - All tensor pointers are DEVICE pointers owned by the caller unless the
+ *     comment says "host".  The library allocates no memory of its own; each
+ *     call takes a caller-owned device workspace `ws` of at least the size the
+ *     matching sv_*_workspace_bytes() returns.  The first 256 bytes of every
+ *     workspace hold the device status word (see sv_read_device_status); a
+ *     fresh workspace must be zero-filled once before first use.  Calls that
+ *     share a workspace must be ordered on one stream.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; nothing synchronises except
+ *     sv_read_device_status and, for non-tail spans, nothing in
+ *     sv_evict_qa_tokens either.  No call allocates, frees or synchronises,
+ *     so every compute call may be captured in a CUDA graph.
+ *   - The return value covers host-side argument checks and the launch
+ *     (cudaGetLastError).  On an error nothing is launched and
+ *     sv_last_error() returns a description (thread-local).
+ *   - Device-side index errors (a block id outside the pool, a visual index
+ *     outside [0, n_vis)) set a bit in the status word; the offending load is
+ *     skipped (read as zero).  Kernels never trap.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16).  Accumulation is
+ *     fp32.  No C++ exception crosses this ABI.
+ *   - GQA: query head h reads KV head h / G with G = H / Hkv.
+ */
+#ifndef SV_H_
+#define SV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,   /* a null pointer, a size out of range, k > n ... */
+  SV_ERR_UNSUPPORTED = 2,   /* a head_dim or shape this build has no kernel for */
+  SV_ERR_CUDA = 3,          /* a CUDA runtime error while launching */
+  SV_ERR_WORKSPACE = 4,     /* ws_bytes smaller than required */
+  SV_ERR_DEVICE_BOUNDS = 5  /* reported by sv_read_device_status only */
+} sv_status;
+
+/* Device status bits (the status word is the first int32 of a workspace). */
+#define SV_DEV_BAD_BLOCK 0x1   /* a block-table entry outside [0, num_blocks) */
+#define SV_DEV_BAD_INDEX 0x2   /* a visual index outside [0, n_vis) */
+
+/* Tokens per KV page (fixed). */
+#define SV_BLOCK_TOKENS 16
+
+const char* sv_status_string(sv_status s);
+/* Thread-local description of the last error returned on this thread. */
+const char* sv_last_error(void);
+/* Library version string, e.g. "sv 0.1 sm_103a". */
+const char* sv_version(void);
+
+/*
+ * One layer's paged KV cache (caller-owned device memory).
+ * k_pool, v_pool: bf16 [num_blocks][n_kv_heads][16][head_dim].  Each page
+ * holds 16 consecutive logical positions of one sequence for every KV head.
+ */
+typedef struct {
+  void* k_pool;
+  void* v_pool;
+  int32_t num_blocks;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+} sv_kv_layer;
+
+/*
+ * A batch of sequences sharing one block table (same table for every layer).
+ * block_table: DEVICE int32 [batch][max_blocks]; logical position t of
+ * sequence b lives in page block_table[b][t / 16], row t % 16.
+ * Logical layout of every sequence: visual tokens at [0, n_vis), then n_text
+ * text tokens.  Lengths are uniform over the batch.
+ */
+typedef struct {
+  const int32_t* block_table;
+  int32_t batch;
+  int32_t max_blocks;
+  int32_t n_vis;
+  int32_t n_text;
+} sv_seq_batch;
+
+/* ------------------------------------------------------------------------
+ * Workspace sizes (bytes, always >= 256).  Pure host functions.
+ */
+size_t sv_salience_workspace_bytes(int B, int H, int N, int d);
+size_t sv_topk_workspace_bytes(int rows, int n, int k);
+size_t sv_prune_workspace_bytes(int B, int N, int k);
+size_t sv_retrieve_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n_vis, int k);
+size_t sv_attn_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n_tokens);
+size_t sv_evict_workspace_bytes(void);
+
+/* ------------------------------------------------------------------------
+ * Prefill salience -- velog.io summary §3.1 (salience table, "no summary
+ * token" encoders such as SigLIP / QwenVL: the intra-visual attention a token
+ * receives, averaged over all tokens; kernel paragraph: softmax normalisation
+ * and salience accumulation streamed without materialising the attention
+ * matrix); xllm-io review §三 salience formula.
+ *
+ *   salience[b][j] = 1/(H*N) * sum_h sum_i softmax_j(scale * q[b,h,i,:] . k[b,h,j,:])
+ *
+ * q, k     : bf16 [B][H][N][d], contiguous.
+ * scale    : logit scale (1/sqrt(d) for standard attention); must be > 0.
+ * salience : out fp32 [B][N]; each row sums to 1.
+ * Supported: d in {64, 72, 128}, 1 <= N <= 4096.  Computed with tcgen05
+ * tensor-core tiles (bf16 operands, fp32 accumulation) in two passes: row
+ * log-sum-exp, then column accumulation.  Deterministic.
+ */
+sv_status sv_salience_prefill(const void* q, const void* k, int B, int H, int N, int d,
+                              float scale, float* salience, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * Row-wise top-k (the selection step shared by prefill pruning and decode
+ * retrieval) -- velog.io summary §3.1 (drop the lowest-salience tokens) and
+ * §3.2 (activate the highest-scoring tokens); xllm-io review §五 topk.
+ *
+ * scores : fp32 [rows][n].
+ * idx    : out int32 [rows][k]: the k largest entries of each row, ties broken
+ *          towards the lower index (-0.0 equals +0.0), written in ascending
+ *          index order.  NaN scores give an unspecified (but valid) choice.
+ * 1 <= k <= n <= 2^24.
+ */
+sv_status sv_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/*
+ * Prefill prune + compaction -- velog.io summary §2 table (prefill tokens are
+ * actually deleted) and §3.1; xllm-io review §五 query_agnostic_pruning.
+ *
+ * salience  : fp32 [B][N] (e.g. from sv_salience_prefill).
+ * feat      : [B][N][row_bytes] opaque rows (row_bytes % 16 == 0, base 16-byte aligned).
+ * feat_out  : out [B][k][row_bytes]: the kept rows in ascending token order.
+ * kept_idx  : out int32 [B][k] ascending.
+ */
+sv_status sv_prune_compact(const float* salience, int B, int N, int k, const void* feat,
+                           int64_t row_bytes, void* feat_out, int32_t* kept_idx, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * Decode query-aware retrieval -- velog.io summary §3.2 "Query-Aware Token
+ * Selection" (text query as Query, cached visual tokens as Keys, aggregate
+ * attention strength; the rest stays cached but inactive); xllm-io review §三
+ * Selected = TopK(Query . KV_Cache, k) and §五 query_aware_retrieval.
+ *
+ *   score[b][g][j] = sum_{r<R} sum_{h in group g} q[b,r,h,:] . K[b,g,j,:],  j < n_vis
+ *   vis_idx[b][g]  = top-k of score[b][g]  (ties -> lower index, ascending)
+ *
+ * q        : bf16 [B][R][H][d] (the current question's query rows).
+ * layer    : the layer's paged cache; seqs: batch view (only n_vis is used).
+ * vis_idx  : out int32 [B][Hkv][k].
+ * scores   : optional out fp32 [B][Hkv][n_vis] (NULL = not written).
+ * Supported: d in {64, 128}; 1 <= k <= n_vis; H % Hkv == 0.
+ */
+sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer,
+                           const sv_seq_batch* seqs, int k, int32_t* vis_idx, float* scores,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Sparse decode attention -- velog.io summary §3.2 (only the query-relevant
+ * subset of the preserved visual cache is read) and §4.5 kernel table
+ * ("decoding attention": reduced KV, less memory traffic).
+ *
+ *   T[b][g] = vis_idx[b][g][0..k) U [n_vis, n_vis + n_text)
+ *   out[b][h] = sum_{t in T} softmax_t(scale * q[b,h] . K[b,g,t]) V[b,g,t],  g = h / G
+ *
+ * q       : bf16 [B][H][d] (one decode query per head).
+ * vis_idx : int32 [B][Hkv][k], distinct values in [0, n_vis); NULL = all
+ *           n_vis visual tokens (dense attention; k is then ignored).
+ * out     : out bf16 [B][H][d].
+ * lse     : optional out fp32 [B][H], log sum_t exp(scale q.k_t) (NULL = none).
+ * Split-K over tokens with an fp32 online softmax; per-split partials live in
+ * ws and are merged by a second kernel.  Supported: d in {64, 128}.
+ */
+sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
+                                const sv_seq_batch* seqs, const int32_t* vis_idx, int k,
+                                void* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Partial KV-cache eviction between rounds -- velog.io summary §4.1 Setup
+ * (after each round only the previous question/answer KV entries are removed;
+ * the visual cache stays); xllm-io review §五 partial_kv_cache_eviction.
+ *
+ * Removes text-relative positions [text_begin, text_end) of every sequence
+ * in every layer.  Visual pages are never touched.  A tail span
+ * (text_end == n_text) only shortens seqs->n_text; otherwise the later text
+ * tokens are moved down on the GPU (one kernel per layer on `stream`).
+ * seqs           : host struct; n_text is updated on success.
+ * n_blocks_in_use: optional host out int32 [batch]: pages each sequence still
+ *                  needs (the caller owns free-page bookkeeping).
+ */
+sv_status sv_evict_qa_tokens(const sv_kv_layer* layers, int n_layers, sv_seq_batch* seqs,
+                             int32_t text_begin, int32_t text_end, int32_t* n_blocks_in_use,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Append T new tokens' K/V at logical positions [n_vis + n_text, + T) of every
+ * sequence (a helper for driving rounds; the caller then adds T to n_text).
+ * k_new, v_new: bf16 [B][T][Hkv][d].  The pages must already be in the table.
+ */
+sv_status sv_kv_append(const sv_kv_layer* layer, const sv_seq_batch* seqs, const void* k_new,
+                       const void* v_new, int T, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Read (and optionally clear) the device status word of a workspace.
+ * Synchronises `stream`.  status_out: host int32 (SV_DEV_* bits, 0 = clean).
+ */
+sv_status sv_read_device_status(void* ws, int clear, int32_t* status_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SV_H_ */
