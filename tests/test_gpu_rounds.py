@@ -1,0 +1,147 @@
+"""GPU parity of the round-boundary operations and of the multi-turn loop:
+append, partial eviction (tail and middle spans), and five question/answer
+rounds of retrieval + 256 sparse decode steps against the oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import assert_attention_close, assert_selection
+from visual_token_sparsity_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def logical(pool, bt, n):
+    return torch.from_numpy(oracle.paged_view(pool.cpu().view(torch.int16).numpy(), bt.cpu().numpy(), n))
+
+
+def make(shape, seed_layer=0):
+    from visual_token_sparsity_gb300 import binding as sv
+    bt = synth.random_block_table(shape.batch, shape.max_blocks, shape.num_blocks,
+                                  seed=synth.subseed(shape.seed, seed_layer, 98))
+    lay = synth.draw_decode_layer(shape, seed_layer, bt.to(DEV), device=DEV)
+    return lay, sv.KvLayer(lay.k_pool, lay.v_pool), sv.SeqBatch(bt.to(DEV), shape.n_vis, shape.n_text)
+
+
+@pytest.mark.parametrize("span", [(20, 40), (0, 40), (5, 6), (0, 1), (10, 10), (3, 37)])
+def test_evict_matches_list_filter(lib, span):
+    from visual_token_sparsity_gb300 import binding as sv
+    shape = synth.DecodeShape("t", H=4, Hkv=2, d=64, n_vis=100, n_text=40, layers=2, batch=2, keep=0.5,
+                              seed=21)
+    layers = []
+    for l in range(2):
+        _, layer, seqs = make(shape, l)
+        layers.append(layer)
+    n0 = shape.n_tokens
+    before = [(logical(l.k_pool, seqs.block_table, n0), logical(l.v_pool, seqs.block_table, n0))
+              for l in layers]
+    used = sv.sv_evict_qa_tokens(layers, seqs, span[0], span[1], sv.workspace(256))
+    torch.cuda.synchronize()
+    assert seqs.n_text == 40 - (span[1] - span[0])
+    assert used == [synth.blocks_for(100 + seqs.n_text)] * 2
+    for l, layer in enumerate(layers):
+        K2, V2, nt = oracle.evict_qa_tokens(before[l][0].numpy(), before[l][1].numpy(), 100, 40,
+                                            span[0], span[1])
+        got_k = logical(layer.k_pool, seqs.block_table, 100 + nt).numpy()
+        got_v = logical(layer.v_pool, seqs.block_table, 100 + nt).numpy()
+        np.testing.assert_array_equal(got_k, K2)
+        np.testing.assert_array_equal(got_v, V2)
+
+
+def test_append_writes_token_rows(lib):
+    from visual_token_sparsity_gb300 import binding as sv
+    shape = synth.DecodeShape("t", H=8, Hkv=4, d=128, n_vis=64, n_text=5, layers=1, batch=3, keep=0.5,
+                              seed=31, extra_blocks=2)
+    lay, layer, seqs = make(shape)
+    kn = synth.normal_bf16((3, 20, 4, 128), 1).to(DEV)
+    vn = synth.normal_bf16((3, 20, 4, 128), 2).to(DEV)
+    sv.sv_kv_append(layer, seqs, kn, vn, sv.workspace(256))
+    torch.cuda.synchronize()
+    K2, V2 = oracle.append_tokens(lay.k_logical.cpu().view(torch.int16).numpy(),
+                                  lay.v_logical.cpu().view(torch.int16).numpy(), 69,
+                                  kn.cpu().view(torch.int16).numpy(), vn.cpu().view(torch.int16).numpy())
+    np.testing.assert_array_equal(logical(layer.k_pool, seqs.block_table, 89).numpy(), K2)
+    np.testing.assert_array_equal(logical(layer.v_pool, seqs.block_table, 89).numpy(), V2)
+
+
+def _round_inputs(shape, r):
+    """Question K/V + rows, then 256 answer tokens' K/V and decode queries."""
+    B, Hkv, H, d = shape.batch, shape.Hkv, shape.H, shape.d
+    s = lambda t: synth.subseed(shape.seed, 100 + r, t)
+    qk = synth.normal_bf16((B, 32, Hkv, d), s(1))
+    qv = synth.normal_bf16((B, 32, Hkv, d), s(2))
+    rows = synth.normal_bf16((B, 32, H, d), s(3))
+    ak = synth.normal_bf16((B, 256, Hkv, d), s(4))
+    av = synth.normal_bf16((B, 256, Hkv, d), s(5))
+    aq = synth.normal_bf16((B, 256, H, d), s(6))
+    return qk, qv, rows, ak, av, aq
+
+
+def _run_round(sv, shape, layer, seqs, r, ws_r, ws_a, ws_e, prefix=32):
+    qk, qv, rows, ak, av, aq = _round_inputs(shape, r)
+    if seqs.n_text > prefix:
+        sv.sv_evict_qa_tokens([layer], seqs, prefix, seqs.n_text, ws_e)
+    sv.sv_kv_append(layer, seqs, qk.to(DEV), qv.to(DEV), ws_e)
+    seqs.n_text += 32
+    vis = torch.empty(shape.batch, shape.Hkv, shape.k, dtype=torch.int32, device=DEV)
+    sc = torch.empty(shape.batch, shape.Hkv, shape.n_vis, device=DEV)
+    sv.sv_retrieve_topk(rows.to(DEV), layer, seqs, shape.k, vis, sc, ws_r)
+    outs = torch.empty(256, shape.batch, shape.H, shape.d, dtype=torch.bfloat16, device=DEV)
+    akd, avd, aqd = ak.to(DEV), av.to(DEV), aq.to(DEV)
+    for t in range(256):
+        sv.sv_kv_append(layer, seqs, akd[:, t:t + 1].contiguous(), avd[:, t:t + 1].contiguous(), ws_e)
+        seqs.n_text += 1
+        sv.sv_sparse_decode_attn(aqd[:, t].contiguous(), 1 / math.sqrt(shape.d), layer, seqs, vis, shape.k,
+                                 outs[t], None, ws_a)
+    torch.cuda.synchronize()
+    return vis, sc, outs
+
+
+def test_multiturn_rounds_match_oracle_and_do_not_leak(lib):
+    from visual_token_sparsity_gb300 import binding as sv
+    shape = synth.multiturn()
+    lay, layer, seqs = make(shape)
+    B, Hkv, H, d = shape.batch, shape.Hkv, shape.H, shape.d
+    ws_r = sv.workspace(sv.sv_retrieve_workspace_bytes(B, H, Hkv, d, shape.n_vis, shape.k))
+    ws_a = sv.workspace(sv.sv_attn_workspace_bytes(B, H, Hkv, d, shape.k + 32 + 32 + 256))
+    ws_e = sv.workspace(256)
+    K = lay.k_logical.cpu().double().numpy()
+    V = lay.v_logical.cpu().double().numpy()
+    n_used = shape.n_tokens
+    first_outs = {}
+    for r in range(5):
+        vis, sc, outs = _run_round(sv, shape, layer, seqs, r, ws_r, ws_a, ws_e)
+        # oracle: evict the previous Q&A, append the question, retrieve, decode
+        qk, qv, rows, ak, av, aq = _round_inputs(shape, r)
+        if n_used > shape.n_vis + 32:
+            K, V, nt = oracle.evict_qa_tokens(K, V, shape.n_vis, n_used - shape.n_vis, 32, n_used - shape.n_vis)
+            n_used = shape.n_vis + nt
+        K, V = oracle.append_tokens(K, V, n_used, qk.double().numpy(), qv.double().numpy())
+        n_used += 32
+        idx_ref, sc_ref = oracle.retrieve_topk(rows.double().numpy(), K[:, :, :shape.n_vis], shape.k)
+        assert_selection(vis.cpu().numpy(), sc_ref, shape.k, f"round {r} retrieval")
+        same = np.array_equal(vis.cpu().numpy(), idx_ref)
+        for t in range(256):
+            K, V = oracle.append_tokens(K, V, n_used, ak[:, t:t + 1].double().numpy(),
+                                        av[:, t:t + 1].double().numpy())
+            n_used += 1
+            if same and (t % 16 == 0 or t == 255):
+                o_ref, _ = oracle.sparse_decode_attention(aq[:, t].double().numpy(), K, V, idx_ref,
+                                                          shape.n_vis, n_used - shape.n_vis)
+                assert_attention_close(outs[t].cpu().numpy(), o_ref, f"round {r} step {t}")
+        first_outs[r] = (vis.clone(), outs.clone())
+        assert sv.sv_read_device_status(ws_a) == 0 and sv.sv_read_device_status(ws_e) == 0
+    # no leakage: round 3 replayed on a cache that never saw rounds 0-2 gives the same bits
+    lay2, layer2, seqs2 = make(shape)
+    vis3, _, outs3 = _run_round(sv, shape, layer2, seqs2, 3, ws_r, ws_a, ws_e)
+    assert torch.equal(vis3, first_outs[3][0])
+    assert torch.equal(outs3, first_outs[3][1])

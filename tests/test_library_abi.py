@@ -1,0 +1,105 @@
+"""CPU checks of the C ABI: libsv.so builds, loads without a GPU, exports every
+function include/sv.h declares (and no other sv_ symbol), and its host-side
+argument checks reject bad calls before anything is launched."""
+
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sv.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    if not shutil.which("nvcc") and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from visual_token_sparsity_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_boundary_calls():
+    names = header_functions()
+    for n in ("sv_salience_prefill", "sv_prune_compact", "sv_retrieve_topk", "sv_sparse_decode_attn",
+              "sv_evict_qa_tokens", "sv_kv_append", "sv_topk_rows", "sv_read_device_status"):
+        assert n in names
+
+
+def test_library_exports_exactly_the_header(so):
+    out = subprocess.run(["nm", "-D", "--defined-only", so], capture_output=True, text=True).stdout
+    exported = sorted(set(re.findall(r"\bT (sv_[a-z0-9_]+)$", out, flags=re.M)))
+    assert exported == header_functions()
+    from visual_token_sparsity_gb300 import binding
+    assert sorted(binding.EXPORTED) == header_functions()
+
+
+def test_library_loads_without_gpu_and_reports_version(so):
+    from visual_token_sparsity_gb300 import binding
+    lib = binding.load(so)
+    assert lib.sv_version().decode().startswith("sv ")
+    assert lib.sv_status_string(4).decode() == "workspace too small"
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_host_validation_rejects_before_launch(so):
+    from visual_token_sparsity_gb300 import binding
+    lib = binding.load(so)
+    s = ctypes.c_void_p(0)
+    # k > n
+    assert lib.sv_topk_rows(_fake(), 2, 10, 11, _fake(), _fake(), 256, s) == 1
+    assert b"k" in lib.sv_last_error()
+    # workspace too small
+    assert lib.sv_topk_rows(_fake(), 2, 10, 5, _fake(), _fake(), 16, s) == 4
+    # misaligned workspace
+    assert lib.sv_topk_rows(_fake(), 2, 10, 5, _fake(), _fake(0x10004), 256, s) == 1
+    # salience: unsupported head dim, bad scale, too large N
+    assert lib.sv_salience_prefill(_fake(), _fake(), 1, 1, 16, 96, 0.1, _fake(), _fake(), 1 << 20, s) == 2
+    assert lib.sv_salience_prefill(_fake(), _fake(), 1, 1, 16, 64, -1.0, _fake(), _fake(), 1 << 20, s) == 1
+    assert lib.sv_salience_prefill(_fake(), _fake(), 1, 1, 4000, 128, 0.1, _fake(), _fake(), 1 << 30, s) == 2
+    # retrieval: k > n_vis, H not a multiple of Hkv, head dim 72 unsupported
+    layer = binding.sv_kv_layer(_fake(), _fake(), 100, 2, 64)
+    seqs = binding.sv_seq_batch(_fake(), 1, 10, 100, 10)
+    args = lambda R, H, k: (_fake(), R, H, ctypes.byref(layer), ctypes.byref(seqs), k, _fake(), None,
+                            _fake(), 1 << 20, s)
+    assert lib.sv_retrieve_topk(*args(1, 4, 101)) == 1
+    assert lib.sv_retrieve_topk(*args(1, 3, 10)) == 1
+    layer72 = binding.sv_kv_layer(_fake(), _fake(), 100, 2, 72)
+    assert lib.sv_retrieve_topk(_fake(), 1, 4, ctypes.byref(layer72), ctypes.byref(seqs), 10, _fake(),
+                                None, _fake(), 1 << 20, s) == 2
+    # lengths beyond the block table
+    seqs_long = binding.sv_seq_batch(_fake(), 1, 10, 150, 20)
+    assert lib.sv_retrieve_topk(_fake(), 1, 4, ctypes.byref(layer), ctypes.byref(seqs_long), 10, _fake(),
+                                None, _fake(), 1 << 20, s) == 1
+    # attention: group size above 8
+    layer1 = binding.sv_kv_layer(_fake(), _fake(), 100, 1, 64)
+    assert lib.sv_sparse_decode_attn(_fake(), 16, 0.1, ctypes.byref(layer1), ctypes.byref(seqs), None, 0,
+                                     _fake(), None, _fake(), 1 << 20, s) == 2
+    # eviction span outside the text
+    assert lib.sv_evict_qa_tokens(ctypes.byref(layer), 1, ctypes.byref(seqs), 5, 11, None, _fake(), 256, s) == 1
+    assert seqs.n_text == 10
+
+
+def test_workspace_sizes_are_monotone_in_tokens(so):
+    from visual_token_sparsity_gb300 import binding
+    lib = binding.load(so)
+    for B, H, Hkv, d in ((1, 32, 32, 128), (16, 32, 32, 128), (8, 28, 4, 128), (1, 4, 2, 64)):
+        prev = 0
+        for n in range(1, 14000, 97):
+            w = lib.sv_attn_workspace_bytes(B, H, Hkv, d, n)
+            assert w >= prev and w >= 256
+            prev = w
+    assert lib.sv_retrieve_workspace_bytes(16, 32, 32, 128, 2880, 720) >= 256 + 16 * 32 * 2880 * 4
+    assert lib.sv_salience_workspace_bytes(256, 16, 729, 72) >= 256 + 256 * 16 * 729 * 4

@@ -1,0 +1,310 @@
+// C-ABI entry points of libsv (declared in include/sv.h): argument checks,
+// workspace layout and kernel launches.  No allocation, no synchronisation
+// (except sv_read_device_status), no exceptions across the boundary.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/sv.h"
+#include "kernels.h"
+
+namespace sv {
+size_t salience_smem_bytes(int N, int d);
+int topk_max_smem_keys();
+}  // namespace sv
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kMaxSmemPerBlock = 232448;  // 227 KB opt-in on sm_100-family parts
+thread_local char g_err[512] = "";
+
+sv_status fail(sv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+sv_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return SV_OK;
+  return fail(SV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int num_sms() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int* status_word(void* ws) { return static_cast<int*>(ws); }
+
+char* after_status(void* ws) { return static_cast<char*>(ws) + kStatusBytes; }
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+sv_status check_ws(void* ws, size_t have, size_t need) {
+  if (!ws) return fail(SV_ERR_INVALID_ARG, "workspace pointer is NULL");
+  if (!aligned16(ws)) return fail(SV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (have < need) return fail(SV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", have, need);
+  return SV_OK;
+}
+
+sv_status check_cache(const sv_kv_layer* L, const sv_seq_batch* S, bool need_v) {
+  if (!L || !S) return fail(SV_ERR_INVALID_ARG, "layer or batch descriptor is NULL");
+  if (!L->k_pool || (need_v && !L->v_pool) || !S->block_table)
+    return fail(SV_ERR_INVALID_ARG, "cache pool or block table pointer is NULL");
+  if (!aligned16(L->k_pool) || (need_v && !aligned16(L->v_pool)))
+    return fail(SV_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
+  if (L->head_dim != 64 && L->head_dim != 128)
+    return fail(SV_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", L->head_dim);
+  if (L->num_blocks <= 0 || L->n_kv_heads <= 0)
+    return fail(SV_ERR_INVALID_ARG, "num_blocks and n_kv_heads must be positive");
+  if ((long long)L->num_blocks * L->n_kv_heads * SV_BLOCK_TOKENS >= 0xffffffffLL)
+    return fail(SV_ERR_UNSUPPORTED, "pool has too many rows for 32-bit row ids");
+  if (S->batch < 0 || S->max_blocks <= 0 || S->n_vis < 0 || S->n_text < 0)
+    return fail(SV_ERR_INVALID_ARG, "negative batch or length");
+  if ((long long)S->n_vis + S->n_text > (long long)S->max_blocks * SV_BLOCK_TOKENS)
+    return fail(SV_ERR_INVALID_ARG, "n_vis + n_text = %d exceeds max_blocks * 16 = %d",
+                S->n_vis + S->n_text, S->max_blocks * SV_BLOCK_TOKENS);
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARG: return "invalid argument";
+    case SV_ERR_UNSUPPORTED: return "unsupported shape";
+    case SV_ERR_CUDA: return "CUDA error";
+    case SV_ERR_WORKSPACE: return "workspace too small";
+    case SV_ERR_DEVICE_BOUNDS: return "device-side index out of bounds";
+  }
+  return "unknown status";
+}
+
+const char* sv_last_error(void) { return g_err; }
+
+const char* sv_version(void) { return "sv 0.1 sm_103a"; }
+
+// ------------------------------------------------------------------ sizes
+
+size_t sv_salience_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0) return kStatusBytes;
+  return kStatusBytes + round256(sv::salience_workspace_bytes(B, H, N, d));
+}
+
+size_t sv_topk_workspace_bytes(int rows, int n, int k) {
+  (void)rows; (void)n; (void)k;
+  return kStatusBytes;
+}
+
+size_t sv_prune_workspace_bytes(int B, int N, int k) {
+  (void)B; (void)N; (void)k;
+  return kStatusBytes;
+}
+
+size_t sv_retrieve_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n_vis, int k) {
+  (void)H; (void)head_dim; (void)k;
+  if (B < 0 || n_kv_heads < 0 || n_vis < 0) return kStatusBytes;
+  return kStatusBytes + round256((size_t)B * n_kv_heads * n_vis * sizeof(float));
+}
+
+size_t sv_attn_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n_tokens) {
+  if (B < 0 || H <= 0 || n_kv_heads <= 0 || head_dim <= 0 || n_tokens < 0 || H % n_kv_heads)
+    return kStatusBytes;
+  const int G = H / n_kv_heads;
+  const sv::AttnPlan p = sv::attn_plan(B, n_kv_heads, G, n_tokens);
+  const size_t parts = (size_t)B * n_kv_heads * p.nsplit_max * G;
+  return kStatusBytes + round256(parts * 2 * sizeof(float)) +
+         round256(parts * head_dim * sizeof(float));
+}
+
+size_t sv_evict_workspace_bytes(void) { return kStatusBytes; }
+
+// ------------------------------------------------------------------ prefill
+
+sv_status sv_salience_prefill(const void* q, const void* k, int B, int H, int N, int d, float scale,
+                              float* salience, void* ws, size_t ws_bytes, void* stream) {
+  if (!q || !k || !salience) return fail(SV_ERR_INVALID_ARG, "q, k and salience must be non-NULL");
+  if (B < 0 || H <= 0 || N <= 0) return fail(SV_ERR_INVALID_ARG, "need B >= 0, H > 0, N > 0");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (d != 64 && d != 72 && d != 128) return fail(SV_ERR_UNSUPPORTED, "salience head_dim %d (64, 72 or 128)", d);
+  if (!aligned16(q) || !aligned16(k)) return fail(SV_ERR_INVALID_ARG, "q and k must be 16-byte aligned");
+  if (sv::salience_smem_bytes(N, d) > kMaxSmemPerBlock)
+    return fail(SV_ERR_UNSUPPORTED, "N = %d too large for resident salience tiles at d = %d", N, d);
+  if ((long long)B * H > 0x7fffffffLL) return fail(SV_ERR_INVALID_ARG, "B * H too large");
+  sv_status s = check_ws(ws, ws_bytes, sv_salience_workspace_bytes(B, H, N, d));
+  if (s != SV_OK) return s;
+  if (B == 0) return SV_OK;
+  cudaError_t e = sv::launch_salience(q, k, B, H, N, d, scale, salience, after_status(ws),
+                                      status_word(ws), num_sms(), static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue)
+    return fail(SV_ERR_CUDA, "tensor-map encoding or launch rejected the salience operands");
+  return cuda_status(e, "sv_salience_prefill");
+}
+
+sv_status sv_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx, void* ws,
+                       size_t ws_bytes, void* stream) {
+  if (!scores || !idx) return fail(SV_ERR_INVALID_ARG, "scores and idx must be non-NULL");
+  if (rows < 0 || n <= 0 || n > (1 << 24)) return fail(SV_ERR_INVALID_ARG, "need rows >= 0, 0 < n <= 2^24");
+  if (k < 1 || k > n) return fail(SV_ERR_INVALID_ARG, "need 1 <= k <= n (k = %d, n = %d)", k, n);
+  sv_status s = check_ws(ws, ws_bytes, sv_topk_workspace_bytes(rows, n, k));
+  if (s != SV_OK) return s;
+  return cuda_status(sv::launch_topk_rows(scores, rows, n, k, idx, static_cast<cudaStream_t>(stream)),
+                     "sv_topk_rows");
+}
+
+sv_status sv_prune_compact(const float* salience, int B, int N, int k, const void* feat,
+                           int64_t row_bytes, void* feat_out, int32_t* kept_idx, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!salience || !kept_idx) return fail(SV_ERR_INVALID_ARG, "salience and kept_idx must be non-NULL");
+  if (B < 0 || N <= 0 || N > (1 << 24)) return fail(SV_ERR_INVALID_ARG, "need B >= 0, 0 < N <= 2^24");
+  if (k < 1 || k > N) return fail(SV_ERR_INVALID_ARG, "need 1 <= k <= N (k = %d, N = %d)", k, N);
+  if (row_bytes < 0 || row_bytes % 16) return fail(SV_ERR_INVALID_ARG, "row_bytes must be a multiple of 16");
+  if (row_bytes > 0 && (!feat || !feat_out)) return fail(SV_ERR_INVALID_ARG, "feat and feat_out must be non-NULL");
+  if (row_bytes > 0 && (!aligned16(feat) || !aligned16(feat_out)))
+    return fail(SV_ERR_INVALID_ARG, "feat and feat_out must be 16-byte aligned");
+  sv_status s = check_ws(ws, ws_bytes, sv_prune_workspace_bytes(B, N, k));
+  if (s != SV_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = sv::launch_topk_rows(salience, B, N, k, kept_idx, st);
+  if (e == cudaSuccess && row_bytes > 0)
+    e = sv::launch_gather_rows(feat, B, N, k, row_bytes, kept_idx, feat_out, status_word(ws), st);
+  return cuda_status(e, "sv_prune_compact");
+}
+
+// ------------------------------------------------------------------ decode
+
+sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer,
+                           const sv_seq_batch* seqs, int k, int32_t* vis_idx, float* scores,
+                           void* ws, size_t ws_bytes, void* stream) {
+  sv_status s = check_cache(layer, seqs, false);
+  if (s != SV_OK) return s;
+  if (!q || !vis_idx) return fail(SV_ERR_INVALID_ARG, "q and vis_idx must be non-NULL");
+  if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  const int Hkv = layer->n_kv_heads;
+  if (R <= 0 || H <= 0 || H % Hkv) return fail(SV_ERR_INVALID_ARG, "need R > 0 and H a multiple of n_kv_heads");
+  if (seqs->n_vis <= 0) return fail(SV_ERR_INVALID_ARG, "no visual tokens to retrieve from");
+  if (k < 1 || k > seqs->n_vis) return fail(SV_ERR_INVALID_ARG, "need 1 <= k <= n_vis (k = %d)", k);
+  s = check_ws(ws, ws_bytes, sv_retrieve_workspace_bytes(seqs->batch, H, Hkv, layer->head_dim, seqs->n_vis, k));
+  if (s != SV_OK) return s;
+  if (seqs->batch == 0) return SV_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* sc = scores ? scores : reinterpret_cast<float*>(after_status(ws));
+  cudaError_t e = sv::launch_retrieve_score(q, R, H, H / Hkv, layer->k_pool, layer->num_blocks, Hkv,
+                                            layer->head_dim, seqs->block_table, seqs->max_blocks,
+                                            seqs->n_vis, seqs->batch, sc, status_word(ws), num_sms(), st);
+  if (e == cudaSuccess) e = sv::launch_topk_rows(sc, seqs->batch * Hkv, seqs->n_vis, k, vis_idx, st);
+  return cuda_status(e, "sv_retrieve_topk");
+}
+
+sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
+                                const sv_seq_batch* seqs, const int32_t* vis_idx, int k, void* out,
+                                float* lse, void* ws, size_t ws_bytes, void* stream) {
+  sv_status s = check_cache(layer, seqs, true);
+  if (s != SV_OK) return s;
+  if (!q || !out) return fail(SV_ERR_INVALID_ARG, "q and out must be non-NULL");
+  if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  const int Hkv = layer->n_kv_heads;
+  if (H <= 0 || H % Hkv) return fail(SV_ERR_INVALID_ARG, "H must be a positive multiple of n_kv_heads");
+  if (H / Hkv > 8) return fail(SV_ERR_UNSUPPORTED, "query heads per KV head %d > 8", H / Hkv);
+  if (!std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale must be finite");
+  const int k_vis = vis_idx ? k : seqs->n_vis;
+  if (vis_idx && (k < 0 || k > seqs->n_vis)) return fail(SV_ERR_INVALID_ARG, "need 0 <= k <= n_vis");
+  const int n_tok = k_vis + seqs->n_text;
+  if (n_tok <= 0) return fail(SV_ERR_INVALID_ARG, "the attended token set is empty");
+  s = check_ws(ws, ws_bytes, sv_attn_workspace_bytes(seqs->batch, H, Hkv, layer->head_dim, n_tok));
+  if (s != SV_OK) return s;
+  if (seqs->batch == 0) return SV_OK;
+  const sv::AttnPlan p = sv::attn_plan(seqs->batch, Hkv, H / Hkv, n_tok);
+  const size_t parts = (size_t)seqs->batch * Hkv * p.nsplit * (H / Hkv);
+  sv::AttnArgs a;
+  a.q = q; a.H = H; a.scale = scale;
+  a.k_pool = layer->k_pool; a.v_pool = layer->v_pool;
+  a.num_blocks = layer->num_blocks; a.Hkv = Hkv; a.D = layer->head_dim;
+  a.block_table = seqs->block_table; a.max_blocks = seqs->max_blocks;
+  a.vis_idx = vis_idx; a.k_vis = k_vis; a.n_vis = seqs->n_vis; a.n_text = seqs->n_text;
+  a.batch = seqs->batch; a.out = out; a.lse = lse;
+  a.part_ml = reinterpret_cast<float*>(after_status(ws));
+  a.part_o = reinterpret_cast<float*>(after_status(ws) + round256(parts * 2 * sizeof(float)));
+  a.status = status_word(ws);
+  return cuda_status(sv::launch_sparse_attn(a, static_cast<cudaStream_t>(stream)), "sv_sparse_decode_attn");
+}
+
+// ------------------------------------------------------------------ rounds
+
+sv_status sv_evict_qa_tokens(const sv_kv_layer* layers, int n_layers, sv_seq_batch* seqs,
+                             int32_t text_begin, int32_t text_end, int32_t* n_blocks_in_use,
+                             void* ws, size_t ws_bytes, void* stream) {
+  if (!layers || !seqs || n_layers < 0) return fail(SV_ERR_INVALID_ARG, "layers and seqs must be non-NULL");
+  if (text_begin < 0 || text_begin > text_end || text_end > seqs->n_text)
+    return fail(SV_ERR_INVALID_ARG, "need 0 <= text_begin <= text_end <= n_text (%d, %d, %d)",
+                text_begin, text_end, seqs->n_text);
+  for (int l = 0; l < n_layers; ++l) {
+    sv_status s = check_cache(&layers[l], seqs, true);
+    if (s != SV_OK) return s;
+  }
+  sv_status s = check_ws(ws, ws_bytes, sv_evict_workspace_bytes());
+  if (s != SV_OK) return s;
+  const int count = seqs->n_text - text_end;   // later text tokens to move down
+  if (text_end > text_begin && count > 0) {
+    for (int l = 0; l < n_layers; ++l) {
+      cudaError_t e = sv::launch_kv_move_down(
+          layers[l].k_pool, layers[l].v_pool, layers[l].num_blocks, layers[l].n_kv_heads,
+          layers[l].head_dim, seqs->block_table, seqs->max_blocks, seqs->batch,
+          seqs->n_vis + text_begin, seqs->n_vis + text_end, count, status_word(ws),
+          static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_status(e, "sv_evict_qa_tokens");
+    }
+  }
+  seqs->n_text -= text_end - text_begin;
+  if (n_blocks_in_use) {
+    const int need = (seqs->n_vis + seqs->n_text + SV_BLOCK_TOKENS - 1) / SV_BLOCK_TOKENS;
+    for (int b = 0; b < seqs->batch; ++b) n_blocks_in_use[b] = need;
+  }
+  return SV_OK;
+}
+
+sv_status sv_kv_append(const sv_kv_layer* layer, const sv_seq_batch* seqs, const void* k_new,
+                       const void* v_new, int T, void* ws, size_t ws_bytes, void* stream) {
+  sv_status s = check_cache(layer, seqs, true);
+  if (s != SV_OK) return s;
+  if (T < 0) return fail(SV_ERR_INVALID_ARG, "T must be >= 0");
+  if (T > 0 && (!k_new || !v_new)) return fail(SV_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+  if (T > 0 && (!aligned16(k_new) || !aligned16(v_new)))
+    return fail(SV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  if ((long long)seqs->n_vis + seqs->n_text + T > (long long)seqs->max_blocks * SV_BLOCK_TOKENS)
+    return fail(SV_ERR_INVALID_ARG, "appending %d tokens overflows the block table", T);
+  s = check_ws(ws, ws_bytes, sv_evict_workspace_bytes());
+  if (s != SV_OK) return s;
+  return cuda_status(sv::launch_kv_append(layer->k_pool, layer->v_pool, layer->num_blocks,
+                                          layer->n_kv_heads, layer->head_dim, seqs->block_table,
+                                          seqs->max_blocks, seqs->batch, seqs->n_vis + seqs->n_text,
+                                          k_new, v_new, T, status_word(ws),
+                                          static_cast<cudaStream_t>(stream)),
+                     "sv_kv_append");
+}
+
+sv_status sv_read_device_status(void* ws, int clear, int32_t* status_out, void* stream) {
+  if (!ws || !status_out) return fail(SV_ERR_INVALID_ARG, "ws and status_out must be non-NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
+  if (e != cudaSuccess) return cuda_status(e, "sv_read_device_status");
+  *status_out = v;
+  return SV_OK;
+}
+
+}  // extern "C"

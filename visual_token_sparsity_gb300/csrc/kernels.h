@@ -1,0 +1,68 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sv {
+
+// ---- retrieval scoring (retrieve.cu)
+cudaError_t launch_retrieve_score(const void* q, int R, int H, int G, const void* k_pool,
+                                  int num_blocks, int Hkv, int D, const int32_t* block_table,
+                                  int max_blocks, int n_vis, int batch, float* scores,
+                                  int* status, int num_sms, cudaStream_t stream);
+
+// ---- row top-k (topk.cu)
+cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
+                             cudaStream_t stream);
+
+// ---- sparse decode attention (attn.cu)
+struct AttnPlan {
+  int tile;
+  int chunk;   // tokens per split (multiple of tile)
+  int nsplit;  // splits per (sequence, KV head)
+  int nsplit_max;  // upper bound of nsplit over all n' <= n_tokens
+};
+AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens);
+
+struct AttnArgs {
+  const void* q;
+  int H;
+  float scale;
+  const void* k_pool;
+  const void* v_pool;
+  int num_blocks, Hkv, D;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* vis_idx;
+  int k_vis, n_vis, n_text, batch;
+  void* out;
+  float* lse;
+  float* part_ml;
+  float* part_o;
+  int* status;
+};
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+
+// ---- compaction gather (prune.cu)
+cudaError_t launch_gather_rows(const void* feat, int B, int N, int k, int64_t row_bytes,
+                               const int32_t* idx, void* out, int* status, cudaStream_t stream);
+
+// ---- cache maintenance (evict.cu)
+cudaError_t launch_kv_move_down(void* k_pool, void* v_pool, int num_blocks, int Hkv, int D,
+                                const int32_t* block_table, int max_blocks, int batch,
+                                int dst_pos, int src_pos, int count, int* status,
+                                cudaStream_t stream);
+cudaError_t launch_kv_append(void* k_pool, void* v_pool, int num_blocks, int Hkv, int D,
+                             const int32_t* block_table, int max_blocks, int batch, int pos0,
+                             const void* k_new, const void* v_new, int T, int* status,
+                             cudaStream_t stream);
+
+// ---- prefill salience (salience.cu)
+size_t salience_workspace_bytes(int B, int H, int N, int d);
+cudaError_t launch_salience(const void* q, const void* k, int B, int H, int N, int d, float scale,
+                            float* salience, void* ws, int* status, int num_sms,
+                            cudaStream_t stream);
+
+}  // namespace sv
