@@ -1,0 +1,446 @@
+"""Benchmark of the SparseVILA hot path on GB300.
+
+Default workload: LLaVA-NeXT-7B-shaped decode (Llama-2-7B attention: 32 MHA
+heads, head_dim 128, 32 layers; paged bf16 KV with 16-token pages; 2880
+visual + 128 text tokens per sequence; batch 16; retrieval keeps 50%).
+One step = one decode step over all 32 layers, each layer running query-aware
+retrieval (1 query row) followed by sparse decode attention over the selected
+visual tokens plus all text tokens.  The step is captured once in a CUDA graph
+and replayed.  Inputs are seeded synthetic tensors (no weights or datasets).
+
+The line also carries the prefill salience figure (SigLIP-so400m shape, 256
+frames of 729 tokens, 16 heads, d 72) in tokens/s and as a fraction of the
+dense bf16 tensor peak.
+
+Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(weak scaling, no collective on the data path).
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+# the CPU oracle leg is timed single-threaded (reported as cores = 1)
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "sparse decode step µs & KV-read GB/s vs HBM peak; salience tokens/s vs TC peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="sv", choices=["sv", "reference"])
+    p.add_argument("--batch", type=int, default=16)
+    p.add_argument("--keep", type=float, default=0.5)
+    p.add_argument("--layers", type=int, default=32)
+    p.add_argument("--salience-batch", type=int, default=256)
+    p.add_argument("--no-salience", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-decode", action="store_true", help="salience measurement only")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, bf16, bf16_sus, src = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = float(d.get("hbm_gbs", hbm))
+            bf16 = float(d.get("bf16_tflops", bf16))
+            bf16_sus = float(d.get("bf16_tflops_sustained", bf16_sus))
+            src = "measured"
+        except Exception:
+            pass
+    return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16_sus, "source": src}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+
+def decode_bytes(shape):
+    """Algorithmic HBM bytes of one decode step (all layers, whole batch)."""
+    d2 = shape.d * 2
+    retrieve = shape.n_vis * shape.Hkv * d2                                # visual keys
+    attend = (shape.k + shape.n_text) * shape.Hkv * d2 * 2 + shape.k * shape.Hkv * 4   # K+V + indices
+    return shape.layers * shape.batch * retrieve, shape.layers * shape.batch * attend
+
+
+class DecodeWorkload:
+    def __init__(self, shape, dev):
+        from visual_token_sparsity_gb300 import binding as sv, synth
+        self.sv, self.shape, self.dev = sv, shape, dev
+        s = shape
+        bt = synth.random_block_table(s.batch, s.max_blocks, s.num_blocks, seed=synth.subseed(s.seed, 0, 99))
+        self.bt = bt.to(dev)
+        self.seqs = sv.SeqBatch(self.bt, s.n_vis, s.n_text)
+        self.layers = []
+        for l in range(s.layers):
+            lay = synth.draw_decode_layer(s, l, self.bt, device=dev)
+            self.layers.append(sv.KvLayer(lay.k_pool, lay.v_pool))
+            del lay
+        qs = [synth.draw_decode_queries(s, l, device=dev) for l in range(s.layers)]
+        self.q_rows = torch.stack([q[0] for q in qs])      # [L][B][1][H][d]
+        self.q_dec = torch.stack([q[1] for q in qs])       # [L][B][H][d]
+        self.vis = torch.empty(s.layers, s.batch, s.Hkv, s.k, dtype=torch.int32, device=dev)
+        self.out = torch.empty(s.layers, s.batch, s.H, s.d, dtype=torch.bfloat16, device=dev)
+        self.ws_r = sv.workspace(sv.sv_retrieve_workspace_bytes(s.batch, s.H, s.Hkv, s.d, s.n_vis, s.k), dev)
+        self.ws_a = sv.workspace(sv.sv_attn_workspace_bytes(s.batch, s.H, s.Hkv, s.d, s.k + s.n_text), dev)
+        self.scale = 1.0 / math.sqrt(s.d)
+        torch.cuda.synchronize()
+
+    def retrieve(self, l, q_rows=None):
+        s = self.shape
+        self.sv.sv_retrieve_topk(self.q_rows[l] if q_rows is None else q_rows, self.layers[l], self.seqs, s.k,
+                                 self.vis[l], None, self.ws_r)
+
+    def attend(self, l, q=None, out=None):
+        s = self.shape
+        self.sv.sv_sparse_decode_attn(self.q_dec[l] if q is None else q, self.scale, self.layers[l], self.seqs,
+                                      self.vis[l], s.k, self.out[l] if out is None else out, None, self.ws_a)
+
+    def step(self):
+        for l in range(self.shape.layers):
+            self.retrieve(l)
+            self.attend(l)
+
+    def attn_only_step(self):
+        for l in range(self.shape.layers):
+            self.attend(l)
+
+
+def time_graph(fn, steps, warmup, stream):
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, warmup)):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
+def replay_timed(g, steps, stream, barrier):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end) / steps      # ms per step
+
+
+def per_call_times(wl, steps, stream):
+    """Average device time of each C-ABI call kind, timed with events on the stream."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    tr, ta = [], []
+    with torch.cuda.stream(stream):
+        for it in range(steps + 2):
+            for l in range(wl.shape.layers):
+                e0, e1, e2 = ev(), ev(), ev()
+                e0.record(stream)
+                wl.retrieve(l)
+                e1.record(stream)
+                wl.attend(l)
+                e2.record(stream)
+                if it >= 2:
+                    tr.append((e0, e1))
+                    ta.append((e1, e2))
+    torch.cuda.synchronize()
+    return (float(np.mean([a.elapsed_time(b) for a, b in tr])), float(np.mean([a.elapsed_time(b) for a, b in ta])))
+
+
+def e2e_throughput(wl, steps, warmup, stream, bytes_step):
+    """Same metric through the public C-ABI with host buffers: per step the
+    queries come from pinned host memory and the attention outputs go back."""
+    s = wl.shape
+    hq_rows = torch.empty_like(wl.q_rows, device="cpu").pin_memory()
+    hq_dec = torch.empty_like(wl.q_dec, device="cpu").pin_memory()
+    hq_rows.copy_(wl.q_rows.cpu())
+    hq_dec.copy_(wl.q_dec.cpu())
+    hout = torch.empty_like(wl.out, device="cpu").pin_memory()
+    dq_rows = torch.empty_like(wl.q_rows)
+    dq_dec = torch.empty_like(wl.q_dec)
+
+    def one():
+        dq_rows.copy_(hq_rows, non_blocking=True)
+        dq_dec.copy_(hq_dec, non_blocking=True)
+        for l in range(s.layers):
+            wl.retrieve(l, dq_rows[l])
+            wl.attend(l, dq_dec[l])
+        hout.copy_(wl.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / steps
+    h2d = hq_rows.numel() * 2 + hq_dec.numel() * 2
+    d2h = hout.numel() * 2
+    return bytes_step / dt / 1e9, h2d, d2h
+
+
+def salience_measure(batch, steps, warmup, stream):
+    from visual_token_sparsity_gb300 import binding as sv, synth
+    ss = synth.siglip_salience(batch=batch)
+    q, k, _ = synth.draw_salience(ss, device="cuda")
+    sal = torch.empty(ss.batch, ss.N, device="cuda")
+    ws = sv.workspace(sv.sv_salience_workspace_bytes(ss.batch, ss.H, ss.N, ss.d))
+    # rotate across copies so that repeated calls read more than L2 holds
+    ncopy = max(1, math.ceil(3 * 129e6 / (2 * q.numel() * 2)))
+    qs = [q] + [q.clone() for _ in range(ncopy - 1)]
+    ks = [k] + [k.clone() for _ in range(ncopy - 1)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            sv.sv_salience_prefill(qs[i % ncopy], ks[i % ncopy], 1 / math.sqrt(ss.d), sal, ws)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(steps):
+            sv.sv_salience_prefill(qs[i % ncopy], ks[i % ncopy], 1 / math.sqrt(ss.d), sal, ws)
+        end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    flops = 4.0 * ss.H * ss.N * ss.N * ss.d * ss.batch
+    return ss, ms, flops
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample_seconds(shape, units, seed=0):
+    """Run the fp64 oracle on `units` (layer, sequence) pairs of the decode
+    workload; returns (seconds, algorithmic bytes covered)."""
+    import oracle
+    from visual_token_sparsity_gb300 import synth
+    one = synth.DecodeShape(shape.name, H=shape.H, Hkv=shape.Hkv, d=shape.d, n_vis=shape.n_vis,
+                            n_text=shape.n_text, layers=1, batch=1, keep=shape.keep, R=shape.R, seed=shape.seed)
+    bt = synth.random_block_table(1, one.max_blocks, one.num_blocks, seed=1, identity=True)
+    total = 0.0
+    rb, ab = decode_bytes(one)
+    for u in range(units):
+        lay = synth.draw_decode_layer(one, u, bt)
+        qr, qd = synth.draw_decode_queries(one, u)
+        K = lay.k_logical.double().numpy()
+        V = lay.v_logical.double().numpy()
+        qr64, qd64 = qr.double().numpy(), qd.double().numpy()
+        t0 = time.perf_counter()
+        idx, _ = oracle.retrieve_topk(qr64, K[:, :, :one.n_vis], one.k)
+        oracle.sparse_decode_attention(qd64, K, V, idx, one.n_vis, one.n_text)
+        total += time.perf_counter() - t0
+    return total, units * (rb + ab)
+
+
+def cpu_baseline(shape, budget_s=10.0):
+    units, secs, nbytes = 0, 0.0, 0
+    while secs < budget_s and units < 1000:
+        t, b = oracle_sample_seconds(shape, 1, seed=units)
+        units += 1
+        secs += t
+        nbytes += b
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{units} (layer, sequence) units of the same workload, retrieval + sparse attention, "
+                      f"fp64 numpy, single thread"}
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    a = parse()
+    rank, world, local = dist_env()
+    from visual_token_sparsity_gb300 import synth
+    shape = synth.llava_next_decode(batch=a.batch, keep=a.keep, layers=a.layers)
+    config = {"workload": f"{shape.name}: {shape.layers} layers, batch {shape.batch}, {shape.H} MHA heads, d {shape.d}, "
+                          f"{shape.n_vis} visual + {shape.n_text} text tokens, page 16, retrieval keep {shape.keep} "
+                          f"(k={shape.k}), 1 query row",
+              "global_batch": shape.batch * world, "layers": shape.layers, "keep": shape.keep,
+              "parallelism": f"replicas x{world}",
+              "l2": "inputs larger than L2 (KV cache %.1f GB per replica)" % (
+                  shape.layers * 2 * shape.num_blocks * shape.Hkv * 16 * shape.d * 2 / 1e9)}
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        for _ in range(a.warmup):
+            oracle_sample_seconds(shape, 1)
+        t, nb = 0.0, 0
+        for i in range(a.steps):
+            dt, b = oracle_sample_seconds(shape, 1, seed=i)
+            t += dt
+            nb += b
+        v = nb / t / 1e9
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": a.gpus,
+                          "steps": a.steps, "warmup": a.warmup, "ms_per_step": t / a.steps * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                           "sample": "each step: one (layer, sequence) unit of the workload, "
+                                                     "retrieval + sparse attention, fp64 numpy, single thread"},
+                          "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(local)
+        barrier = lambda: dist.barrier(device_ids=[local])
+    else:
+        torch.cuda.set_device(0)
+        barrier = lambda: None
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+    __graft_entry__.build()
+    pk = peaks()
+
+    stream = torch.cuda.Stream()
+    line = {"metric": METRIC, "value": None, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) K/V with 2% x4 outliers, random page tables)",
+            "config": config}
+    if not a.no_decode:
+        decode_measure(a, shape, dev, stream, barrier, world, pk, line)
+    if not a.no_salience:
+        ss, sms, flops = salience_measure(a.salience_batch, max(3, a.steps // 2), 3, stream)
+        tf = flops / (sms * 1e-3) / 1e12
+        line["salience"] = {"workload": f"{ss.name}: {ss.batch} frames x {ss.N} tokens, {ss.H} heads, d {ss.d}",
+                            "ms": sms, "tokens_per_s": ss.batch * ss.N / (sms * 1e-3),
+                            "tflops": tf, "bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": tf / pk["bf16_tflops"], "peak_source": pk["source"],
+                            "flop_count": "4*H*N^2*d per frame (both QK^T passes, d unpadded)"}
+    if rank == 0:
+        if world == 1 and not a.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(shape)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
+    rb, ab = decode_bytes(shape)
+    bytes_step = rb + ab
+    wl = DecodeWorkload(shape, dev)
+    g_step = time_graph(wl.step, a.steps, max(3, a.warmup), stream)
+    g_attn = time_graph(wl.attn_only_step, a.steps, 3, stream)
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = replay_timed(g_step, a.steps, stream, barrier)
+    ms_attn = replay_timed(g_attn, a.steps, stream, barrier)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, ms_attn], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_attn = t.tolist()
+    value = world * bytes_step / (ms * 1e-3) / 1e9
+
+    t_ret, t_att = per_call_times(wl, max(3, a.steps // 4), stream)
+    per_launch_ret = rb / (shape.layers)
+    per_launch_att = ab / (shape.layers)
+    if t_att >= t_ret:
+        dom = ("sv_sparse_decode_attn (split-K gather attention + combine)", per_launch_att, t_att)
+    else:
+        dom = ("sv_retrieve_topk (paged GEMV + radix top-k)", per_launch_ret, t_ret)
+    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+
+    line.update({"value": value, "ms_per_step": ms, "decode_step_us": ms * 1e3,
+            "attn_only_step_us": ms_attn * 1e3,
+            "clocks": clk.summary(),
+            "gpu_launches": a.steps * shape.layers * 4,
+            "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
+                         "traffic": None,
+                         "per_call_us": {"retrieve": t_ret * 1e3, "attention": t_att * 1e3}},
+            "hbm_frac_step": (bytes_step / (ms * 1e-3) / 1e9) / pk["hbm_gbs"]})
+
+    if not a.no_e2e:
+        e2e, h2d, d2h = e2e_throughput(wl, max(3, a.steps // 2), 2, stream, bytes_step)
+        line["e2e"] = {"value": world * e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del wl, g_step, g_attn
+    torch.cuda.empty_cache()
+
+
+if __name__ == "__main__":
+    main()

@@ -20,6 +20,7 @@ Tolerances (stated once, used everywhere):
 """
 
 import numpy as np
+import torch
 
 ATTN_ABS = 1e-2
 ATTN_REL = 2e-2
@@ -30,8 +31,14 @@ SCORE_REL = 1e-5
 TIE_REL = 1e-3
 
 
+def _f64(x):
+    if isinstance(x, torch.Tensor):
+        return x.detach().double().cpu().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
 def assert_attention_close(got, ref, what="attention"):
-    got = np.asarray(got, dtype=np.float64)
+    got = _f64(got)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref).max()
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)

@@ -238,7 +238,7 @@ def test_sparse_attention_matches_oracle(lib, H, Hkv, d, n_vis, n_text, B, k, so
     out, lse = run_attn(shape, layer, seqs, qd, vis, k)
     o_ref, l_ref = oracle.sparse_decode_attention(f64(qd), f64(lay.k_logical), f64(lay.v_logical),
                                                   vis.numpy(), n_vis, n_text)
-    assert_attention_close(out.cpu().numpy(), o_ref)
+    assert_attention_close(out, o_ref)
     assert np.abs(lse.cpu().numpy() - l_ref).max() <= LSE_ABS
 
 
@@ -250,11 +250,11 @@ def test_dense_attention_when_index_list_is_null(lib):
     out, lse = run_attn(shape, layer, seqs, qd, None, 0)
     o_ref, l_ref = oracle.sparse_decode_attention(f64(qd), f64(lay.k_logical), f64(lay.v_logical),
                                                   None, 300, 21)
-    assert_attention_close(out.cpu().numpy(), o_ref)
+    assert_attention_close(out, o_ref)
     # k = n_vis through the index path gives the same numbers
     allidx = torch.arange(300, dtype=torch.int32).expand(2, 2, 300).contiguous()
     out2, _ = run_attn(shape, layer, seqs, qd, allidx, 300)
-    assert_attention_close(out2.cpu().numpy(), o_ref)
+    assert_attention_close(out2, o_ref)
 
 
 def test_attention_paging_invariance_bitwise(lib):
@@ -327,7 +327,7 @@ def test_llava_next_full_batch_sampled(lib, keep):
                                                       shape.n_vis, shape.n_text)
         # the GPU attended over its own selection; where that equals the oracle's, compare outputs
         if np.array_equal(vis[b, g].cpu().numpy(), idx_ref[0, 0]):
-            assert_attention_close(out[b, g].cpu().numpy(), o_ref[0, 0], f"attention b{b} g{g}")
+            assert_attention_close(out[b, g], o_ref[0, 0], f"attention b{b} g{g}")
             assert abs(lse[b, g].item() - l_ref[0, 0]) <= LSE_ABS
 
 
@@ -354,4 +354,4 @@ def test_longvila_full_batch_sampled(lib):
         full_idx = vis.clone()
         full_idx[b, g] = torch.from_numpy(idx_ref[0, 0].astype(np.int32)).to(DEV)
         o2, _ = run_attn(shape, layer, seqs, qd, full_idx, shape.k, with_lse=False)
-        assert_attention_close(o2[b, g * G:(g + 1) * G].cpu().numpy(), o_ref[0], f"attention b{b} g{g}")
+        assert_attention_close(o2[b, g * G:(g + 1) * G], o_ref[0], f"attention b{b} g{g}")

@@ -137,7 +137,7 @@ def test_multiturn_rounds_match_oracle_and_do_not_leak(lib):
             if same and (t % 16 == 0 or t == 255):
                 o_ref, _ = oracle.sparse_decode_attention(aq[:, t].double().numpy(), K, V, idx_ref,
                                                           shape.n_vis, n_used - shape.n_vis)
-                assert_attention_close(outs[t].cpu().numpy(), o_ref, f"round {r} step {t}")
+                assert_attention_close(outs[t], o_ref, f"round {r} step {t}")
         first_outs[r] = (vis.clone(), outs.clone())
         assert sv.sv_read_device_status(ws_a) == 0 and sv.sv_read_device_status(ws_e) == 0
     # no leakage: round 3 replayed on a cache that never saw rounds 0-2 gives the same bits
