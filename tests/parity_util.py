@@ -2,8 +2,12 @@
 
 Tolerances (stated once, used everywhere):
 
-* Attention outputs (bf16 out, fp32 accumulation): max |gpu - ref| <= 1e-2 and
-  ||gpu - ref||_2 / ||ref||_2 <= 2e-2, per call.
+* Attention outputs (bf16 out, fp32 accumulation): |gpu - ref| <= 1e-2 +
+  2^-8 |ref| elementwise and ||gpu - ref||_2 / ||ref||_2 <= 2e-2, per call.
+  The 2^-8 |ref| term is the final round-to-nearest into the bf16 output
+  (at least half a bf16 ULP at |ref|): outlier-dominated heads reach |out| ~ 12,
+  where one bf16 ULP is 0.0625, so an absolute 1e-2 can only bound the
+  arithmetic before that rounding.
 * lse (fp32): |gpu - ref| <= 1e-3 (natural-log units).
 * Salience (fp32 accumulation of exp over <= 4096 terms, bf16-exact inputs,
   fp32 tensor-core logits): per entry |gpu - ref| / ref <= 1e-4, and every
@@ -24,6 +28,7 @@ import torch
 
 ATTN_ABS = 1e-2
 ATTN_REL = 2e-2
+BF16_HALF_ULP_REL = 2.0 ** -8
 LSE_ABS = 1e-3
 SAL_REL = 1e-4
 SAL_SUM = 1e-5
@@ -40,9 +45,11 @@ def _f64(x):
 def assert_attention_close(got, ref, what="attention"):
     got = _f64(got)
     ref = np.asarray(ref, dtype=np.float64)
-    err = np.abs(got - ref).max()
+    excess = np.abs(got - ref) - BF16_HALF_ULP_REL * np.abs(ref)
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-    assert err <= ATTN_ABS, f"{what}: max abs err {err:.3g} > {ATTN_ABS}"
+    i = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= ATTN_ABS, (f"{what}: |err| {abs(got[i] - ref[i]):.3g} at |ref| {abs(ref[i]):.3g} "
+                                      f"exceeds 1e-2 + 2^-8 |ref|; rel l2 {rel:.3g}")
     assert rel <= ATTN_REL, f"{what}: rel l2 err {rel:.3g} > {ATTN_REL}"
 
 
