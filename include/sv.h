@@ -14,16 +14,17 @@
  * General conventions (every call):
  *   - All tensor pointers are DEVICE pointers owned by the caller unless the
  *     comment says "host".  The library allocates no memory of its own; each
- *     call takes a caller-owned device workspace `ws` of at least the size the
- *     matching sv_*_workspace_bytes() returns.  The first 256 bytes of every
+ *     call (except sv_retrieve_topk_noalloc) takes a caller-owned device
+ *     workspace `ws` of at least the size the matching
+ *     sv_*_workspace_bytes() returns.  The first 256 bytes of every
  *     workspace hold the device status word (see sv_read_device_status); a
  *     fresh workspace must be zero-filled once before first use.  Calls that
  *     share a workspace must be ordered on one stream.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously; nothing synchronises except
  *     sv_read_device_status and, for non-tail spans, nothing in
- *     sv_evict_qa_tokens either.  No call allocates, frees or synchronises,
- *     so every compute call may be captured in a CUDA graph.
+ *     sv_evict_qa_tokens either.  No call allocates, frees or synchronises;
+ *     the workspace-taking compute calls may be captured in a CUDA graph.
  *   - The return value covers host-side argument checks and the launch
  *     (cudaGetLastError).  On an error nothing is launched and
  *     sv_last_error() returns a description (thread-local).
@@ -169,6 +170,36 @@ sv_status sv_prune_compact(const float* salience, int B, int N, int k, const voi
 sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer,
                            const sv_seq_batch* seqs, int k, int32_t* vis_idx, float* scores,
                            void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * sv_retrieve_topk without a workspace.  (No counterpart on the SparseVILA
+ * pages: this is a calling convenience, not part of the method.)
+ *
+ * Some callers cannot allocate device memory at all -- for example a plugin
+ * running inside a host framework that owns all device memory through its
+ * own pool, or a latency-critical loop where cudaMalloc (which can
+ * synchronise the device) is forbidden -- so they cannot supply the scores
+ * workspace sv_retrieve_topk needs.  This entry point computes exactly what
+ * sv_retrieve_topk computes, with the same kernels, keeping the scores in a
+ * fixed scratch array compiled into the library (8 MiB + 256 B of device
+ * memory on every GPU that loads the library, held until the process exits).
+ *
+ * Arguments are those of sv_retrieve_topk minus ws / ws_bytes.  It allocates
+ * nothing and calls no allocating routine.
+ * Limit: batch * n_kv_heads * n_vis <= 2^21 (2,097,152 scores); larger calls
+ * return SV_ERR_WORKSPACE without launching.
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * All calls share the one scratch array: calls that can overlap on the GPU
+ * (different streams without ordering, or several host threads) race and
+ * must not be issued.  The status word at the start of the scratch is
+ * cleared by every call; device-side index errors are skipped as in
+ * sv_retrieve_topk but cannot be read back through sv_read_device_status.
+ */
+sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const sv_kv_layer* layer,
+                                   const sv_seq_batch* seqs, int k, int32_t* vis_idx, float* scores,
+                                   void* stream);
 
 /*
  * Sparse decode attention -- velog.io summary §3.2 (only the query-relevant

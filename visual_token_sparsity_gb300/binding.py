@@ -56,6 +56,8 @@ _SIGS = {
     "sv_prune_compact": (_I, [_VP, _I, _I, _I, _VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
     "sv_retrieve_topk": (_I, [_VP, _I, _I, ctypes.POINTER(sv_kv_layer),
                               ctypes.POINTER(sv_seq_batch), _I, _VP, _VP, _VP, _SZ, _VP]),
+    "sv_retrieve_topk_noalloc": (_I, [_VP, _I, _I, ctypes.POINTER(sv_kv_layer),
+                                      ctypes.POINTER(sv_seq_batch), _I, _VP, _VP, _VP]),
     "sv_sparse_decode_attn": (_I, [_VP, _I, _F, ctypes.POINTER(sv_kv_layer),
                                    ctypes.POINTER(sv_seq_batch), _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
     "sv_evict_qa_tokens": (_I, [ctypes.POINTER(sv_kv_layer), _I, ctypes.POINTER(sv_seq_batch),
@@ -217,6 +219,16 @@ def sv_retrieve_topk(q, layer, seqs, k, vis_idx, scores, ws, stream=None):
     _check(lib.sv_retrieve_topk(_ptr(q, torch.bfloat16, "q"), R, H, ctypes.byref(layer.c),
                                 ctypes.byref(seqs.c), k, _ptr(vis_idx, torch.int32, "vis_idx"),
                                 _ptr(scores, torch.float32, "scores"), *_ws(ws), _stream(stream)))
+
+
+def sv_retrieve_topk_noalloc(q, layer, seqs, k, vis_idx, scores=None, stream=None):
+    """As sv_retrieve_topk, for callers that cannot allocate: no workspace; the
+    library's fixed device scratch holds the scores (limit B * Hkv * n_vis <= 2^21)."""
+    lib = load()
+    B, R, H, d = q.shape
+    _check(lib.sv_retrieve_topk_noalloc(_ptr(q, torch.bfloat16, "q"), R, H, ctypes.byref(layer.c),
+                                        ctypes.byref(seqs.c), k, _ptr(vis_idx, torch.int32, "vis_idx"),
+                                        _ptr(scores, torch.float32, "scores"), _stream(stream)))
 
 
 def sv_sparse_decode_attn(q, scale, layer, seqs, vis_idx, k, out, lse, ws, stream=None):

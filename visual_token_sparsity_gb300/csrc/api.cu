@@ -78,6 +78,11 @@ sv_status check_cache(const sv_kv_layer* L, const sv_seq_batch* S, bool need_v) 
 
 }  // namespace
 
+namespace sv {
+// Records `msg` as this thread's sv_last_error() text.
+void set_error_message(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+}  // namespace sv
+
 extern "C" {
 
 const char* sv_status_string(sv_status s) {
