@@ -47,16 +47,19 @@ def up_to_date():
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force=False, verbose=False, extra_flags=()):
-    """Compile and link libsv.so; returns its path."""
-    if not force and up_to_date():
+def build(force=False, verbose=False, extra_flags=(), out_dir=None):
+    """Compile and link libsv.so (into ``out_dir``, default the package's
+    _lib/); returns its path."""
+    lib_path = LIB if out_dir is None else os.path.join(out_dir, "libsv.so")
+    if not force and out_dir is None and up_to_date():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    obj_dir = OUT_DIR if out_dir is None else out_dir
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,13 +70,13 @@ def build(force=False, verbose=False, extra_flags=()):
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link of libsv.so failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

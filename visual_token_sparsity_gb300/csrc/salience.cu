@@ -8,13 +8,17 @@
 //   s[b][j] = 1/(H N) sum_h sum_i exp(scale q_i.k_j - lse_i),
 //   lse_i   = log sum_j exp(scale q_i.k_j).
 //
-// Design (one CTA per (frame, head), 8 softmax warps + 1 TMA/MMA warp):
+// Design (one CTA per (frame, head), 16 softmax warps + 1 TMA/MMA warp):
 //   pass 1  K_h resident in shared memory, 128-row tiles of Q_h streamed by
 //           TMA; S = Q_tile K^T (M=128, N<=256 per MMA, K=d padded to 16) goes
 //           to a double-buffered TMEM accumulator; every softmax thread owns
-//           one query row (one TMEM lane) and half of the columns, keeps an
-//           online max / sum of exp2, and the two halves are merged into
+//           one query row (one TMEM lane) and a quarter of the columns, keeps
+//           an online max / sum of exp2, and the four parts are merged into
 //           lse_i (log2 domain) in shared memory.
+//   The element-wise work is exp-bound: it uses packed fp32x2 FMA/ADD, a
+//   3-input max tree, independent accumulators, and sends a fixed fraction
+//   of the exponentials to an FMA-pipe polynomial (fastmath.cuh) so that
+//   MUFU and the FMA pipe share the load.
 //   pass 2  Q_h resident, 128-row tiles of K_h streamed; S^T = K_tile Q^T puts
 //           one key per TMEM lane, so the column sum over queries becomes a
 //           per-thread row sum of exp2(z - lse_i) with lse_i broadcast from
@@ -27,13 +31,21 @@
 // a fixed order (deterministic).
 #include "common.cuh"
 #include "kernels.h"
+#include "fastmath.cuh"
 #include "tc_ptx.cuh"
 
 namespace sv {
 
 namespace {
 
-constexpr int kSoftWarps = 8;
+constexpr int kSoftWarps = 16;
+constexpr int kParts = kSoftWarps / 4;   // column parts per TMEM lane quarter
+constexpr int kPartCols = 256 / kParts;  // columns of a 256-column chunk per warp
+#ifndef SV_SAL_POLY_PAIRS
+#define SV_SAL_POLY_PAIRS 0
+#endif
+// of every 16 element pairs, this many take exp2 on the FMA pipe, the rest on MUFU
+constexpr int kPolyPairs = SV_SAL_POLY_PAIRS;
 constexpr int kThreads = (kSoftWarps + 1) * 32;
 constexpr int kTileRows = 128;
 constexpr int kChunkCols = 256;
@@ -61,7 +73,7 @@ SalGeom sal_geom(int N, int d) {
   g.nchunks = (g.Np + kChunkCols - 1) / kChunkCols;
   g.res_bytes = (size_t)g.Rr * g.Kp * 2;
   g.slot_bytes = (size_t)kTileRows * g.Kp * 2;
-  g.smem_bytes = 1024 + g.res_bytes + 2 * g.slot_bytes + (size_t)g.Rr * 4 + 4 * 256 * 4;
+  g.smem_bytes = 1024 + g.res_bytes + 2 * g.slot_bytes + (size_t)g.Rr * 4 + 2 * kParts * 256 * 4;
   return g;
 }
 
@@ -101,7 +113,7 @@ __device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, SalShar
   }
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -113,8 +125,8 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
   const int Kp = a.Kp, Rr = a.Rr;
   uint8_t* res = smem;
   uint8_t* slot[2] = {smem + (size_t)Rr * Kp * 2, smem + (size_t)Rr * Kp * 2 + kTileRows * Kp * 2};
-  float* lse2 = reinterpret_cast<float*>(slot[1] + kTileRows * Kp * 2);
-  float* mrg = lse2 + Rr;
+  float* nlse2 = reinterpret_cast<float*>(slot[1] + kTileRows * Kp * 2);
+  float* mrg = nlse2 + Rr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x;
@@ -208,42 +220,64 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
     }
   } else {
     // ------------------------------------------------ softmax warps
-    const int quarter = warp & 3, half = warp >> 2;
+    // warp w reads TMEM lane quarter (w & 3) -- the hardware ties a warp to the
+    // lanes 32 * (w % 4) .. + 31 -- and the 64-column part (w >> 2) of a chunk.
+    const int quarter = warp & 3, part = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const float sl2 = a.sl2;
+    const uint64_t sl2x2 = fm::splat2(sl2);
     uint32_t u = 0;
-    uint32_t r[32];
+    uint32_t r[64];
     // pass 1: row log-sum-exp (log2 domain)
     for (int t = 0; t < a.nt; ++t) {
+      const bool live = t * kTileRows + quarter * 32 < a.N;
       float m = -INFINITY, l = 0.f;
       for (int c = 0; c < a.nchunks; ++c, ++u) {
         const uint32_t buf = u & 1;
         wait_bar(&sh.bar_full[buf], (u >> 1) & 1, sh);
         ptx::tc_fence_after();
         const int nc = min(kChunkCols, a.Np - kChunkCols * c);
-        const int c1 = min(nc, half * 128 + 128);
-        for (int col = half * 128; col < c1; col += 32) {
-          ptx::tmem_ld32(tbase + lane_addr + buf * kChunkCols + col, r);
+        const int col0 = part * kPartCols;
+        const int ncols = live ? max(0, min(kPartCols, nc - col0)) : 0;
+        if (ncols > 0) {
+          const uint32_t ta = tbase + lane_addr + buf * kChunkCols + col0;
+          ptx::tmem_ld32(ta, r);
+          if (ncols > 32) ptx::tmem_ld32(ta + 32, r + 32);
           ptx::tmem_wait_ld(r);
-          const int key0 = kChunkCols * c + col;
-          float cm = -INFINITY;
-          if (key0 + 32 <= a.N) {
+          if (ncols > 32) ptx::tmem_wait_ld(r + 32);
+          for (int g = 0; g < ncols; g += 32) {
+            uint32_t* v = r + g;
+            const int key0 = kChunkCols * c + col0 + g;
+            if (key0 + 32 > a.N) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) cm = fmaxf(cm, __uint_as_float(r[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (key0 + i >= a.N) r[i] = __float_as_uint(-INFINITY);
-              cm = fmaxf(cm, __uint_as_float(r[i]));
+              for (int i = 0; i < 32; ++i)
+                if (key0 + i >= a.N) v[i] = __float_as_uint(-INFINITY);
             }
-          }
-          const float mn = fmaxf(m, cm * sl2);
-          if (mn != -INFINITY) {
-            float sum = 0.f;
+            float mx[11];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sum += fast_exp2(fmaf(__uint_as_float(r[i]), sl2, -mn));
-            l = l * fast_exp2(m - mn) + sum;
+            for (int i = 0; i < 10; ++i)
+              mx[i] = fm::max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
+                               __uint_as_float(v[3 * i + 2]));
+            mx[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+            const float cm = fmaxf(fm::max3(fm::max3(mx[0], mx[1], mx[2]), fm::max3(mx[3], mx[4], mx[5]),
+                                            fm::max3(mx[6], mx[7], mx[8])),
+                                   fmaxf(mx[9], mx[10]));
+            const float mn = fmaxf(m, cm * sl2);
+            if (mn == -INFINITY) continue;
+            const uint64_t nmn = fm::splat2(-mn);
+            uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int pr = 0; pr < 16; ++pr) {
+              const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
+                                          sl2x2, nmn);
+              const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
+              acc[pr & 3] = fm::add2(acc[pr & 3], e);
+            }
+            const uint64_t s2 = fm::add2(fm::add2(acc[0], acc[1]), fm::add2(acc[2], acc[3]));
+            float s0, s1;
+            fm::unpack2(s2, s0, s1);
+            l = l * fm::ex2_mufu(m - mn) + (s0 + s1);
             m = mn;
           }
         }
@@ -251,52 +285,72 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
       }
-      float* mg = mrg + (t & 1) * 512;
-      mg[half * 256 + row * 2] = m;
-      mg[half * 256 + row * 2 + 1] = l;
+      float* mg = mrg + (t & 1) * (kParts * 256);
+      mg[part * 256 + row * 2] = m;
+      mg[part * 256 + row * 2 + 1] = l;
       softmax_bar();
-      if (half == 0) {
-        const float m1 = mg[256 + row * 2], l1 = mg[256 + row * 2 + 1];
-        const float M = fmaxf(m, m1);
-        const float L = (m == -INFINITY ? 0.f : l * fast_exp2(m - M)) +
-                        (m1 == -INFINITY ? 0.f : l1 * fast_exp2(m1 - M));
+      if (part == 0) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) M = fmaxf(M, mg[p2 * 256 + row * 2]);
+        float L = 0.f;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) {
+          const float mp = mg[p2 * 256 + row * 2];
+          if (mp != -INFINITY) L += mg[p2 * 256 + row * 2 + 1] * fm::ex2_mufu(mp - M);
+        }
         const int qi = t * kTileRows + row;
-        lse2[qi] = qi < a.N ? M + __log2f(L) : INFINITY;
+        // stored negated: pass 2 adds it with one packed FMA; padded queries
+        // get -inf and contribute nothing
+        nlse2[qi] = qi < a.N ? -(M + __log2f(L)) : -INFINITY;
       }
     }
     softmax_bar();
     // pass 2: column sums of exp2(z - lse), one key per TMEM lane
     for (int t = 0; t < a.nt; ++t) {
-      float acc = 0.f;
+      const bool live = t * kTileRows + quarter * 32 < a.N;
+      uint64_t acc[4] = {0, 0, 0, 0};
       for (int c = 0; c < a.nchunks; ++c, ++u) {
         const uint32_t buf = u & 1;
         wait_bar(&sh.bar_full[buf], (u >> 1) & 1, sh);
         ptx::tc_fence_after();
         const int nc = min(kChunkCols, a.Np - kChunkCols * c);
-        const int c1 = min(nc, half * 128 + 128);
-        for (int col = half * 128; col < c1; col += 32) {
-          ptx::tmem_ld32(tbase + lane_addr + buf * kChunkCols + col, r);
+        const int col0 = part * kPartCols;
+        const int ncols = live ? max(0, min(kPartCols, nc - col0)) : 0;
+        if (ncols > 0) {
+          const uint32_t ta = tbase + lane_addr + buf * kChunkCols + col0;
+          ptx::tmem_ld32(ta, r);
+          if (ncols > 32) ptx::tmem_ld32(ta + 32, r + 32);
           ptx::tmem_wait_ld(r);
-          const float4* lp = reinterpret_cast<const float4*>(lse2 + kChunkCols * c + col);
+          if (ncols > 32) ptx::tmem_wait_ld(r + 32);
+          for (int g = 0; g < ncols; g += 32) {
+            const uint32_t* v = r + g;
+            const uint64_t* nl = reinterpret_cast<const uint64_t*>(nlse2 + kChunkCols * c + col0 + g);
 #pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4) {
-            const float4 L = lp[i4];
-            acc += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 0]), sl2, -L.x));
-            acc += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 1]), sl2, -L.y));
-            acc += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 2]), sl2, -L.z));
-            acc += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 3]), sl2, -L.w));
+            for (int pr = 0; pr < 16; ++pr) {
+              const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
+                                          sl2x2, nl[pr]);
+              const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
+              acc[pr & 3] = fm::add2(acc[pr & 3], e);
+            }
           }
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
       }
-      float* mg = mrg + (t & 1) * 512;
-      mg[half * 128 + row] = acc;
+      const uint64_t s2 = fm::add2(fm::add2(acc[0], acc[1]), fm::add2(acc[2], acc[3]));
+      float s0, s1;
+      fm::unpack2(s2, s0, s1);
+      float* mg = mrg + (t & 1) * (kParts * 128);
+      mg[part * 128 + row] = s0 + s1;
       softmax_bar();
-      if (half == 0) {
+      if (part == 0) {
         const int key = t * kTileRows + row;
-        if (key < a.N) a.colsum[(size_t)unit * a.N + key] = acc + mg[128 + row];
+        float tot = 0.f;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) tot += mg[p2 * 128 + row];
+        if (key < a.N) a.colsum[(size_t)unit * a.N + key] = tot;
       }
     }
   }
