@@ -428,7 +428,9 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
     line.update({"value": value, "ms_per_step": ms, "decode_step_us": ms * 1e3,
             "attn_only_step_us": ms_attn * 1e3,
             "clocks": clk.summary(),
-            "gpu_launches": a.steps * shape.layers * 4,
+            # per layer: fused retrieval (+ a separate top-k when the row exceeds
+            # the in-kernel limit) and the fused split-K attention
+            "gpu_launches": a.steps * shape.layers * ((1 if shape.n_vis <= 11264 else 2) + 1),
             "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
                          "traffic": None,

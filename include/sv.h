@@ -182,8 +182,9 @@ sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer
  * own pool, or a latency-critical loop where cudaMalloc (which can
  * synchronise the device) is forbidden -- so they cannot supply the scores
  * workspace sv_retrieve_topk needs.  This entry point computes exactly what
- * sv_retrieve_topk computes, with the same kernels, keeping the scores in a
- * fixed scratch array compiled into the library (8 MiB + 256 B of device
+ * sv_retrieve_topk computes (the same scoring kernel and the same top-k
+ * routine, here always run as a separate top-k kernel), keeping the scores in
+ * a fixed scratch array compiled into the library (8 MiB + 256 B of device
  * memory on every GPU that loads the library, held until the process exits).
  *
  * Arguments are those of sv_retrieve_topk minus ws / ws_bytes.  It allocates

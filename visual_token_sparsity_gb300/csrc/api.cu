@@ -121,7 +121,9 @@ size_t sv_prune_workspace_bytes(int B, int N, int k) {
 size_t sv_retrieve_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n_vis, int k) {
   (void)H; (void)head_dim; (void)k;
   if (B < 0 || n_kv_heads < 0 || n_vis < 0) return kStatusBytes;
-  return kStatusBytes + round256((size_t)B * n_kv_heads * n_vis * sizeof(float));
+  // status | per-row completion counters [B][Hkv] | scores [B][Hkv][n_vis]
+  return kStatusBytes + round256((size_t)B * n_kv_heads * sizeof(int)) +
+         round256((size_t)B * n_kv_heads * n_vis * sizeof(float));
 }
 
 size_t sv_attn_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n_tokens) {
@@ -130,7 +132,8 @@ size_t sv_attn_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n
   const int G = H / n_kv_heads;
   const sv::AttnPlan p = sv::attn_plan(B, n_kv_heads, G, n_tokens);
   const size_t parts = (size_t)B * n_kv_heads * p.nsplit_max * G;
-  return kStatusBytes + round256(parts * 2 * sizeof(float)) +
+  // status | per-(sequence, KV head) split counters | (m, l) partials | o partials
+  return kStatusBytes + round256((size_t)B * n_kv_heads * sizeof(int)) + round256(parts * 2 * sizeof(float)) +
          round256(parts * head_dim * sizeof(float));
 }
 
@@ -205,11 +208,12 @@ sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer
   if (s != SV_OK) return s;
   if (seqs->batch == 0) return SV_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* sc = scores ? scores : reinterpret_cast<float*>(after_status(ws));
-  cudaError_t e = sv::launch_retrieve_score(q, R, H, H / Hkv, layer->k_pool, layer->num_blocks, Hkv,
-                                            layer->head_dim, seqs->block_table, seqs->max_blocks,
-                                            seqs->n_vis, seqs->batch, sc, status_word(ws), num_sms(), st);
-  if (e == cudaSuccess) e = sv::launch_topk_rows(sc, seqs->batch * Hkv, seqs->n_vis, k, vis_idx, st);
+  const size_t rows = (size_t)seqs->batch * Hkv;
+  int* row_done = reinterpret_cast<int*>(after_status(ws));
+  float* sc = scores ? scores : reinterpret_cast<float*>(after_status(ws) + round256(rows * sizeof(int)));
+  cudaError_t e = sv::launch_retrieve(q, R, H, H / Hkv, layer->k_pool, layer->num_blocks, Hkv,
+                                      layer->head_dim, seqs->block_table, seqs->max_blocks, seqs->n_vis,
+                                      seqs->batch, sc, status_word(ws), num_sms(), row_done, k, vis_idx, st);
   return cuda_status(e, "sv_retrieve_topk");
 }
 
@@ -240,8 +244,12 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
   a.block_table = seqs->block_table; a.max_blocks = seqs->max_blocks;
   a.vis_idx = vis_idx; a.k_vis = k_vis; a.n_vis = seqs->n_vis; a.n_text = seqs->n_text;
   a.batch = seqs->batch; a.out = out; a.lse = lse;
-  a.part_ml = reinterpret_cast<float*>(after_status(ws));
-  a.part_o = reinterpret_cast<float*>(after_status(ws) + round256(parts * 2 * sizeof(float)));
+  // the counters' offset depends only on the batch shape, so a workspace
+  // reused with other token counts finds them where the last call zeroed them
+  const size_t cnt_bytes = round256((size_t)seqs->batch * Hkv * sizeof(int));
+  a.split_done = reinterpret_cast<int*>(after_status(ws));
+  a.part_ml = reinterpret_cast<float*>(after_status(ws) + cnt_bytes);
+  a.part_o = reinterpret_cast<float*>(after_status(ws) + cnt_bytes + round256(parts * 2 * sizeof(float)));
   a.status = status_word(ws);
   return cuda_status(sv::launch_sparse_attn(a, static_cast<cudaStream_t>(stream)), "sv_sparse_decode_attn");
 }

@@ -13,8 +13,9 @@
 // the block table, the warp issues all K and V row loads (16 B per lane, whole
 // 128/256-byte rows per lane group) and then folds the per-lane partial dot
 // products with a butterfly reduce-scatter.  The G query heads of the group
-// share every K/V load.  Per-split (m, l, o) partials go to the workspace and
-// a second kernel merges them.
+// share every K/V load.  Per-split (m, l, o) partials go to the workspace; the
+// last warp to finish a (sequence, KV head) -- a device-scope counter, no
+// waiting -- merges them and writes the bf16 output and the lse.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -63,13 +64,14 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32)
+__global__ void __launch_bounds__(kAttnWarps * 32, (G == 1 ? 3 : 1))
 sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
                          const uint16_t* __restrict__ k_pool, const uint16_t* __restrict__ v_pool,
                          int num_blocks, int Hkv, const int32_t* __restrict__ block_table,
                          int max_blocks, const int32_t* __restrict__ vis_idx, int k_vis,
                          int n_vis, int n_text, float scale_log2, int batch, int nsplit, int chunk,
-                         float* __restrict__ part_ml, float* __restrict__ part_o, int* status) {
+                         float* __restrict__ part_ml, float* __restrict__ part_o, int* status,
+                         int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse) {
   using S = AttnShape<D, G>;
   constexpr int LPT = S::LPT, TPI = S::TPI, TILE = S::TILE, NL = S::NL, DUP = S::DUP;
 
@@ -218,59 +220,42 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
       part_ml[(pi + hh) * 2 + 1] = lsum[hh];
     }
   }
-}
 
-// Merge the per-split partials of one (sequence, query head).
-__global__ void __launch_bounds__(128)
-attn_combine_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o, int H,
-                    int Hkv, int G, int D, int nsplit, uint16_t* __restrict__ out,
-                    float* __restrict__ lse) {
-  extern __shared__ float wsh[];   // nsplit weights
-  __shared__ float red[32];
-  __shared__ float bc_M, bc_L;
-  const int bh = blockIdx.x;
-  const int b = bh / H, h = bh % H;
-  const int g = h / G, hh = h % G;
-  const size_t base = ((size_t)b * Hkv + g) * nsplit;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-
-  float mx = -INFINITY;
-  for (int s = tid; s < nsplit; s += blockDim.x) mx = fmaxf(mx, part_ml[((base + s) * G + hh) * 2]);
-  mx = warp_max(mx);
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  if (tid == 0) {
+  // The last warp to finish this (sequence, KV head) merges every split:
+  // out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, M = max_s m_s.
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(split_done + bg, 1) == nsplit - 1;
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  constexpr int DPL = D / 32;   // output dims per lane
+  const size_t base = (size_t)bg * nsplit;
+  for (int hh = 0; hh < G; ++hh) {
     float M = -INFINITY;
-    for (int i = 0; i < nw; ++i) M = fmaxf(M, red[i]);
-    bc_M = M;
+    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, __ldcg(part_ml + ((base + s) * G + hh) * 2));
+    M = warp_max(M);
+    float L = 0.f, acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < nsplit; ++s) {
+      const size_t ps = (base + s) * G + hh;
+      const float ms = __ldcg(part_ml + ps * 2);
+      const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
+      L = fmaf(w, __ldcg(part_ml + ps * 2 + 1), L);
+      const float* po = part_o + ps * D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(w, __ldcg(po + e), acc[e]);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint16_t* dst = out + ((size_t)b * H + g * G + hh) * D + lane * DPL;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) dst[e] = (uint16_t)f32_to_bf16_bits(acc[e] * inv);
+    if (lse != nullptr && lane == 0)
+      lse[(size_t)b * H + g * G + hh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
-  __syncthreads();
-  const float M = bc_M;
-  float lacc = 0.f;
-  for (int s = tid; s < nsplit; s += blockDim.x) {
-    const float ms = part_ml[((base + s) * G + hh) * 2];
-    const float wgt = (M == -INFINITY || ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
-    wsh[s] = wgt;
-    lacc += wgt * part_ml[((base + s) * G + hh) * 2 + 1];
-  }
-  lacc = warp_sum(lacc);
-  __syncthreads();
-  if (lane == 0) red[warp] = lacc;
-  __syncthreads();
-  if (tid == 0) {
-    float L = 0.f;
-    for (int i = 0; i < nw; ++i) L += red[i];
-    bc_L = L;
-  }
-  __syncthreads();
-  const float L = bc_L;
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  for (int e = tid; e < D; e += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < nsplit; ++s) acc = fmaf(wsh[s], part_o[((base + s) * G + hh) * D + e], acc);
-    out[(size_t)bh * D + e] = (uint16_t)f32_to_bf16_bits(acc * inv);
-  }
-  if (lse && tid == 0) lse[bh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  if (lane == 0) split_done[bg] = 0;   // ready for the next call
 }
 
 template <int D, int G>
@@ -281,7 +266,7 @@ static void launch_split(const AttnArgs& a, const AttnPlan& p, cudaStream_t stre
       static_cast<const uint16_t*>(a.q), a.H, static_cast<const uint16_t*>(a.k_pool),
       static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks,
       a.vis_idx, a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk,
-      a.part_ml, a.part_o, a.status);
+      a.part_ml, a.part_o, a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse);
 }
 
 template <int D>
@@ -304,13 +289,6 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const AttnPlan p = attn_plan(a.batch, a.Hkv, G, a.k_vis + a.n_text);
   const bool ok = a.D == 128 ? dispatch_g<128>(a, p, stream) : dispatch_g<64>(a, p, stream);
   if (!ok) return cudaErrorInvalidValue;
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const size_t smem = (size_t)p.nsplit * sizeof(float);
-  attn_combine_kernel<<<a.batch * a.H, 128, smem, stream>>>(a.part_ml, a.part_o, a.H, a.Hkv, G,
-                                                             a.D, p.nsplit,
-                                                             static_cast<uint16_t*>(a.out), a.lse);
   return cudaGetLastError();
 }
-
 }  // namespace sv

@@ -7,11 +7,13 @@
 
 namespace sv {
 
-// ---- retrieval scoring (retrieve.cu)
-cudaError_t launch_retrieve_score(const void* q, int R, int H, int G, const void* k_pool,
-                                  int num_blocks, int Hkv, int D, const int32_t* block_table,
-                                  int max_blocks, int n_vis, int batch, float* scores,
-                                  int* status, int num_sms, cudaStream_t stream);
+// ---- retrieval scoring + top-k (retrieve.cu).  With row_done (zeroed int per
+// (sequence, KV head) row) and rows that fit in shared memory, the top-k runs
+// inside the scoring kernel; otherwise a separate top-k kernel follows.
+cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_pool, int num_blocks,
+                            int Hkv, int D, const int32_t* block_table, int max_blocks, int n_vis,
+                            int batch, float* scores, int* status, int num_sms, int* row_done, int k,
+                            int32_t* vis_idx, cudaStream_t stream);
 
 // ---- row top-k (topk.cu)
 cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
@@ -41,6 +43,7 @@ struct AttnArgs {
   float* lse;
   float* part_ml;
   float* part_o;
+  int* split_done;   // zeroed int per (sequence, KV head); left zeroed after the call
   int* status;
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);

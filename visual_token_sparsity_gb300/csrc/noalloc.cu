@@ -5,8 +5,9 @@
 // own pool, or a latency-critical loop in which cudaMalloc (which may
 // synchronise the device and take driver locks) is not allowed.  They cannot
 // provide the scores workspace that sv_retrieve_topk needs.  This variant runs
-// the same two kernels (paged scoring GEMV, then row top-k) with the scores
-// kept in a fixed scratch array that lives in this library's device image.
+// the same scoring kernel and top-k routine (here as two kernels: paged
+// scoring GEMV, then row top-k) with the scores kept in a fixed scratch array
+// that lives in this library's device image.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its kNoAllocScratchBytes until the process exits.  Host code
@@ -103,11 +104,10 @@ extern "C" sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const
   if (e == cudaSuccess) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    e = sv::launch_retrieve_score(q, R, H, H / Hkv, layer->k_pool, layer->num_blocks, Hkv, layer->head_dim,
-                                  seqs->block_table, seqs->max_blocks, seqs->n_vis, seqs->batch, sc, status,
-                                  sms, st);
+    e = sv::launch_retrieve(q, R, H, H / Hkv, layer->k_pool, layer->num_blocks, Hkv, layer->head_dim,
+                            seqs->block_table, seqs->max_blocks, seqs->n_vis, seqs->batch, sc, status, sms,
+                            nullptr, k, vis_idx, st);
   }
-  if (e == cudaSuccess) e = sv::launch_topk_rows(sc, seqs->batch * Hkv, seqs->n_vis, k, vis_idx, st);
   if (e != cudaSuccess) return noalloc_fail(SV_ERR_CUDA, "sv_retrieve_topk_noalloc: %s", cudaGetErrorString(e));
   return SV_OK;
 }

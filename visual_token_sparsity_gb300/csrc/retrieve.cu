@@ -1,35 +1,62 @@
-// Query-aware retrieval scoring (decode phase).
+// Query-aware retrieval (decode phase): scoring GEMV fused with the top-k.
 //
 // velog.io SparseVILA summary §3.2 "Query-Aware Token Selection": the current
 // question's query rows are scored against every cached visual key; xllm-io
 // review §三: Selected = TopK(Query . KV_Cache, k).  The score of visual token
 // j for KV head g is sum_r sum_{h in g} q[r,h] . K[g,j]; by linearity the
-// query rows and the group's heads are summed first (q_bar), so the kernel is
-// one GEMV per (sequence, KV head) that streams the visual keys once.
+// query rows and the group's heads are summed first (q_bar), so scoring is one
+// GEMV per (sequence, KV head) row that streams the visual keys once.
 //
-// Memory-bound: each KV page of one head (16 tokens x d bf16, 2 or 4 KB,
-// contiguous) is read by one warp with 16-byte loads; the per-lane partial dot
-// products are folded with a butterfly reduce-scatter so the shuffle count per
-// page is ~d/8 instead of 16 * log2(d/8).
+// Memory-bound.  A CTA scores a contiguous run of KV pages of one row; each
+// warp reads whole pages (16 tokens x d bf16, 2 or 4 KB, contiguous) with
+// 16-byte loads and folds the per-lane partial dot products with a butterfly
+// reduce-scatter (~d/8 shuffles per page).  One page in flight per warp at 32
+// registers (64 warps per SM) measured faster than a register-prefetched
+// second page at 104 registers.  The CTA that finishes a row last
+// (a device-scope counter per row, no waiting) runs the exact block top-k on
+// that row's scores while other rows are still streaming, so no separate
+// selection kernel and no extra launch is needed when the row fits in shared
+// memory.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk_block.cuh"
 
 namespace sv {
 
+#ifndef SV_RET_PREFETCH
+#define SV_RET_PREFETCH 0      // 1: keep the next page in flight (more registers, fewer warps)
+#endif
+#ifndef SV_RET_THREADS
+#define SV_RET_THREADS 256
+#endif
+#ifndef SV_RET_WAVES
+#define SV_RET_WAVES 16        // target CTAs = SMs x this
+#endif
+
+namespace {
+constexpr int kRetrieveThreads = SV_RET_THREADS;
+constexpr int kFuseMaxN = 11264;   // keys in dynamic shared memory (44 KB; static + dynamic < 48 KB)
+}  // namespace
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kRetrieveThreads)
 retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
                       const uint16_t* __restrict__ k_pool, int num_blocks, int Hkv,
                       const int32_t* __restrict__ block_table, int max_blocks, int n_vis,
-                      int blocks_per_cta, float* __restrict__ scores, int* status) {
+                      int blocks_per_cta, float* __restrict__ scores, int* status,
+                      int* row_done, int k, int32_t* __restrict__ vis_idx) {
   constexpr int LPT = D / 8;        // lanes per token row (16 B each)
   constexpr int TPI = 32 / LPT;     // tokens per warp-wide load
   constexpr int NL = kBlockTokens / TPI;  // loads per lane per page
   static_assert(NL * 2 == LPT, "page fold assumes two lanes per reduced value");
 
+  extern __shared__ uint32_t topk_keys[];
   __shared__ float qbar[D];
+  __shared__ TopkShared ts;
+  __shared__ int s_last;
   const int g = blockIdx.y;
   const int b = blockIdx.z;
+  const int row = b * Hkv + g;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -39,8 +66,8 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   for (int e = tid; e < D; e += blockDim.x) {
     float acc = 0.f;
     for (int r = 0; r < R; ++r) {
-      const uint16_t* row = q + (((size_t)b * R + r) * H + (size_t)g * G) * D + e;
-      for (int hh = 0; hh < G; ++hh) acc += __uint_as_float((uint32_t)row[(size_t)hh * D] << 16);
+      const uint16_t* qr = q + (((size_t)b * R + r) * H + (size_t)g * G) * D + e;
+      for (int hh = 0; hh < G; ++hh) acc += __uint_as_float((uint32_t)qr[(size_t)hh * D] << 16);
     }
     qbar[e] = acc;
   }
@@ -55,25 +82,30 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   const int blk_begin = blockIdx.x * blocks_per_cta;
   const int blk_end = min(n_vblocks, blk_begin + blocks_per_cta);
   const int32_t* bt = block_table + (size_t)b * max_blocks;
-  float* out = scores + ((size_t)b * Hkv + g) * n_vis;
+  float* out = scores + (size_t)row * n_vis;
   // token held by this lane after the fold
   const int my_tok = ((lane % LPT) >> 1) * TPI + lane / LPT;
 
-  for (int blk = blk_begin + warp; blk < blk_end; blk += nwarps) {
+  auto load_page = [&](int blk, uint4* kv) {
     const int page = __ldg(bt + blk);
     const bool ok = page >= 0 && page < num_blocks;
     if (!ok && lane == 0) flag_status(status, kStatusBadBlock);
     const uint16_t* base = k_pool + (((size_t)(ok ? page : 0) * Hkv + g) * kBlockTokens) * D;
-    uint4 kv[NL];
 #pragma unroll
-    for (int i = 0; i < NL; ++i) {
-      if (ok) kv[i] = ld_stream16(base + (size_t)(lane + 32 * i) * 8);
-      else kv[i] = make_uint4(0, 0, 0, 0);
-    }
+    for (int i = 0; i < NL; ++i)
+      kv[i] = ok ? ld_stream16(base + (size_t)(lane + 32 * i) * 8) : make_uint4(0, 0, 0, 0);
+  };
+
+  uint4 cur[NL], nxt[NL];
+  int blk = blk_begin + warp;
+  if (SV_RET_PREFETCH && blk < blk_end) load_page(blk, cur);
+  for (; blk < blk_end; blk += nwarps) {
+    if (!SV_RET_PREFETCH) load_page(blk, cur);
+    else if (blk + nwarps < blk_end) load_page(blk + nwarps, nxt);
     float part[NL];
 #pragma unroll
     for (int i = 0; i < NL; ++i) {
-      const uint32_t w[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
+      const uint32_t w[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
       float a = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -85,30 +117,56 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
     GroupReduce<NL, LPT>::run(part, lane);
     const int pos = blk * kBlockTokens + my_tok;
     if ((lane & 1) == 0 && pos < n_vis) out[pos] = part[0];
+    if (SV_RET_PREFETCH) {
+#pragma unroll
+      for (int i = 0; i < NL; ++i) cur[i] = nxt[i];
+    }
   }
+
+  if (row_done == nullptr) return;
+  // last CTA of this row selects its top-k
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(row_done + row, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  block_topk_row(out, n_vis, k, vis_idx + (size_t)row * k, topk_keys, ts);
+  if (tid == 0) row_done[row] = 0;   // ready for the next call
 }
 
-cudaError_t launch_retrieve_score(const void* q, int R, int H, int G, const void* k_pool,
-                                  int num_blocks, int Hkv, int D, const int32_t* block_table,
-                                  int max_blocks, int n_vis, int batch, float* scores,
-                                  int* status, int num_sms, cudaStream_t stream) {
+bool retrieve_fuses_topk(int n_vis) { return n_vis <= kFuseMaxN; }
+
+cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_pool, int num_blocks,
+                            int Hkv, int D, const int32_t* block_table, int max_blocks, int n_vis,
+                            int batch, float* scores, int* status, int num_sms, int* row_done, int k,
+                            int32_t* vis_idx, cudaStream_t stream) {
   const int n_vblocks = (n_vis + kBlockTokens - 1) / kBlockTokens;
-  const long long tasks = (long long)batch * Hkv * n_vblocks;
-  // aim for ~16 resident warps' worth of pages per SM, at least 8 pages per CTA
-  long long per = (tasks + (long long)num_sms * 16 - 1) / ((long long)num_sms * 16);
-  int blocks_per_cta = (int)(per < 8 ? 8 : per);
-  if (blocks_per_cta > n_vblocks) blocks_per_cta = n_vblocks;
-  dim3 grid((n_vblocks + blocks_per_cta - 1) / blocks_per_cta, Hkv, batch);
-  dim3 block(256);
+  const int rows = batch * Hkv;
+  // about two waves of 8-warp CTAs over the GPU, at least one page per warp
+  const long long target = (long long)num_sms * SV_RET_WAVES;
+  long long chunks = (target + rows - 1) / rows;
+  int per = (int)((n_vblocks + chunks - 1) / chunks);
+  if (per < 8) per = 8;
+  if (per > n_vblocks) per = n_vblocks;
+  const int grid_x = (n_vblocks + per - 1) / per;
+  const bool fuse = row_done != nullptr && retrieve_fuses_topk(n_vis);
+  const size_t smem = fuse ? (size_t)n_vis * sizeof(uint32_t) : 0;
+  dim3 grid(grid_x, Hkv, batch);
   const uint16_t* qq = static_cast<const uint16_t*>(q);
   const uint16_t* kp = static_cast<const uint16_t*>(k_pool);
+  int* done = fuse ? row_done : nullptr;
   if (D == 128)
-    retrieve_score_kernel<128><<<grid, block, 0, stream>>>(qq, R, H, G, kp, num_blocks, Hkv,
-        block_table, max_blocks, n_vis, blocks_per_cta, scores, status);
+    retrieve_score_kernel<128><<<grid, kRetrieveThreads, smem, stream>>>(
+        qq, R, H, G, kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
+        vis_idx);
   else
-    retrieve_score_kernel<64><<<grid, block, 0, stream>>>(qq, R, H, G, kp, num_blocks, Hkv,
-        block_table, max_blocks, n_vis, blocks_per_cta, scores, status);
-  return cudaGetLastError();
+    retrieve_score_kernel<64><<<grid, kRetrieveThreads, smem, stream>>>(
+        qq, R, H, G, kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
+        vis_idx);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || fuse) return e;
+  return launch_topk_rows(scores, rows, n_vis, k, vis_idx, stream);
 }
 
 }  // namespace sv
