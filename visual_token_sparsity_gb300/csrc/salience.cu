@@ -38,7 +38,10 @@ namespace sv {
 
 namespace {
 
-constexpr int kSoftWarps = 16;
+#ifndef SV_SAL_SOFT_WARPS
+#define SV_SAL_SOFT_WARPS 16
+#endif
+constexpr int kSoftWarps = SV_SAL_SOFT_WARPS;
 constexpr int kParts = kSoftWarps / 4;   // column parts per TMEM lane quarter
 constexpr int kPartCols = 256 / kParts;  // columns of a 256-column chunk per warp
 #ifndef SV_SAL_POLY_PAIRS
@@ -98,8 +101,10 @@ struct SalShared {
   int abort_flag;
 };
 
-// Bounded wait: returns immediately once the CTA has aborted.
+// Bounded wait: returns immediately once the CTA has aborted.  The timer is
+// read only when the phase is not already complete (reading it is slow).
 __device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, SalShared& sh) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = ptx::global_timer();
   for (uint32_t it = 0;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return;
@@ -113,7 +118,7 @@ __device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, SalShar
   }
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -221,147 +226,156 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
   } else {
     // ------------------------------------------------ softmax warps
     // warp w reads TMEM lane quarter (w & 3) -- the hardware ties a warp to the
-    // lanes 32 * (w % 4) .. + 31 -- and the 64-column part (w >> 2) of every
-    // 256-column chunk, as two 32-column groups.  The chunks of both passes
-    // form one sequence; the TMEM load of the next group is always in flight
-    // while the current group is processed.
+    // lanes 32 * (w % 4) .. + 31 -- and the column part (w >> 2) of a chunk.
     const int quarter = warp & 3, part = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const float sl2 = a.sl2;
     const uint64_t sl2x2 = fm::splat2(sl2);
-    const int per_pass = a.nt * a.nchunks;
-    const int total = 2 * per_pass;
-    // 32-column groups of this warp in chunk use v (0, 1 or 2)
-    auto groups = [&](int v) -> int {
-      const int rem = v % per_pass;
-      const int t = rem / a.nchunks, c = rem % a.nchunks;
-      if (t * kTileRows + quarter * 32 >= a.N) return 0;       // rows / keys all padding
-      const int nc = min(kChunkCols, a.Np - kChunkCols * c);
-      return max(0, min(kPartCols, nc - part * kPartCols)) / 32;
-    };
-    auto col_addr = [&](int v) -> uint32_t {
-      return tbase + lane_addr + (uint32_t)(v & 1) * kChunkCols + part * kPartCols;
-    };
-
-    float m = -INFINITY, l = 0.f;            // pass 1 row state (log2 domain)
-    uint64_t acc[4] = {0, 0, 0, 0};          // pass 2 column sums (4 packed accumulators)
-
-    // pass 1 group: stale running max; rescale only when the group max exceeds
-    // it by more than 2^8 (keeps every exp2 argument <= 8)
-    auto rowsum_group = [&](uint32_t* v, int key0) {
-      if (key0 + 32 > a.N) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key0 + i >= a.N) v[i] = __float_as_uint(-INFINITY);
-      }
-      float mx[11];
-#pragma unroll
-      for (int i = 0; i < 10; ++i)
-        mx[i] = fm::max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
-      mx[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
-      const float cm = fmaxf(fm::max3(fm::max3(mx[0], mx[1], mx[2]), fm::max3(mx[3], mx[4], mx[5]),
-                                      fm::max3(mx[6], mx[7], mx[8])),
-                             fmaxf(mx[9], mx[10])) * sl2;
-      if (cm > m + 8.0f) {
-        l = l * fm::ex2_mufu(m - cm);
-        m = cm;
-      }
-      if (m == -INFINITY) return;
-      const uint64_t nm = fm::splat2(-m);
-      uint64_t s4[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int pr = 0; pr < 16; ++pr) {
-        const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])), sl2x2, nm);
-        const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
-        s4[pr & 3] = fm::add2(s4[pr & 3], e);
-      }
-      float s0, s1;
-      fm::unpack2(fm::add2(fm::add2(s4[0], s4[1]), fm::add2(s4[2], s4[3])), s0, s1);
-      l += s0 + s1;
-    };
-    // pass 2 group: exp2(z - lse_query) summed per key
-    auto colsum_group = [&](const uint32_t* v, int q0) {
-      const uint64_t* nl = reinterpret_cast<const uint64_t*>(nlse2 + q0);
-#pragma unroll
-      for (int pr = 0; pr < 16; ++pr) {
-        const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])), sl2x2, nl[pr]);
-        const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
-        acc[pr & 3] = fm::add2(acc[pr & 3], e);
-      }
-    };
-    auto process = [&](uint32_t* v, int pass, int col) {
-      if (pass == 0) rowsum_group(v, col);
-      else colsum_group(v, col);
-    };
-
+    uint32_t u = 0;
     uint32_t ra[32], rb[32];
-    wait_bar(&sh.bar_full[0], 0, sh);
-    ptx::tc_fence_after();
-    if (groups(0) > 0) {
-      ptx::tmem_ld32(col_addr(0), ra);
+    // Runs fn(group registers, column offset) on the warp's ng 32-column
+    // groups starting at TMEM address ta, with the next group's TMEM load in
+    // flight while the current one is processed.
+    auto for_groups = [&](uint32_t ta, int ng, auto&& fn) {
+      if (ng <= 0) return;
+      ptx::tmem_ld32(ta, ra);
       ptx::tmem_wait_ld(ra);
-    }
-    for (int v = 0; v < total; ++v) {
-      const int pass = v / per_pass, rem = v % per_pass;
-      const int t = rem / a.nchunks, c = rem % a.nchunks;
-      const int ng = groups(v);
-      const int col = kChunkCols * c + part * kPartCols;
-      if (ng == 2) ptx::tmem_ld32(col_addr(v) + 32, rb);
-      if (ng >= 1) process(ra, pass, col);
-      if (ng == 2) ptx::tmem_wait_ld(rb);
-      // every TMEM read of this chunk has landed: hand the buffer back
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[v & 1]);
-      const int ng_next = v + 1 < total ? groups(v + 1) : 0;
-      if (v + 1 < total) {
-        wait_bar(&sh.bar_full[(v + 1) & 1], ((v + 1) >> 1) & 1, sh);
+      if (ng > 1) ptx::tmem_ld32(ta + 32, rb);
+      fn(ra, 0);
+      if (ng > 1) {
+        ptx::tmem_wait_ld(rb);
+        if (ng > 2) ptx::tmem_ld32(ta + 64, ra);
+        fn(rb, 32);
+      }
+      if (ng > 2) {
+        ptx::tmem_wait_ld(ra);
+        if (ng > 3) ptx::tmem_ld32(ta + 96, rb);
+        fn(ra, 64);
+      }
+      if (ng > 3) {
+        ptx::tmem_wait_ld(rb);
+        fn(rb, 96);
+      }
+    };
+    // pass 1: row log-sum-exp (log2 domain)
+    for (int t = 0; t < a.nt; ++t) {
+      const bool live = t * kTileRows + quarter * 32 < a.N;
+      float m = -INFINITY, l = 0.f;
+      for (int c = 0; c < a.nchunks; ++c, ++u) {
+        const uint32_t buf = u & 1;
+        wait_bar(&sh.bar_full[buf], (u >> 1) & 1, sh);
         ptx::tc_fence_after();
-        if (ng_next > 0) ptx::tmem_ld32(col_addr(v + 1), ra);
-      }
-      if (ng == 2) process(rb, pass, col + 32);
-      if (c == a.nchunks - 1) {
-        if (pass == 0) {
-          float* mg = mrg + (t & 1) * (kParts * 256);
-          mg[part * 256 + row * 2] = m;
-          mg[part * 256 + row * 2 + 1] = l;
-          softmax_bar();
-          if (part == 0) {
-            float M = -INFINITY;
+        const int nc = min(kChunkCols, a.Np - kChunkCols * c);
+        const int col0 = part * kPartCols;
+        const int ncols = live ? max(0, min(kPartCols, nc - col0)) : 0;
+        {
+          const uint32_t ta = tbase + lane_addr + buf * kChunkCols + col0;
+          for_groups(ta, ncols >> 5, [&](uint32_t* v, int g) {
+            const int key0 = kChunkCols * c + col0 + g;
+            if (key0 + 32 > a.N) {
 #pragma unroll
-            for (int p2 = 0; p2 < kParts; ++p2) M = fmaxf(M, mg[p2 * 256 + row * 2]);
-            float L = 0.f;
-#pragma unroll
-            for (int p2 = 0; p2 < kParts; ++p2) {
-              const float mp = mg[p2 * 256 + row * 2];
-              if (mp != -INFINITY) L += mg[p2 * 256 + row * 2 + 1] * fm::ex2_mufu(mp - M);
+              for (int i = 0; i < 32; ++i)
+                if (key0 + i >= a.N) v[i] = __float_as_uint(-INFINITY);
             }
-            const int qi = t * kTileRows + row;
-            // stored negated for the packed FMA of pass 2; padded queries get
-            // -inf and contribute nothing
-            nlse2[qi] = qi < a.N ? -(M + __log2f(L)) : -INFINITY;
-          }
-          m = -INFINITY;
-          l = 0.f;
-          if (t == a.nt - 1) softmax_bar();   // all of lse visible before pass 2
-        } else {
-          float s0, s1;
-          fm::unpack2(fm::add2(fm::add2(acc[0], acc[1]), fm::add2(acc[2], acc[3])), s0, s1);
-          float* mg = mrg + (t & 1) * (kParts * 128);
-          mg[part * 128 + row] = s0 + s1;
-          softmax_bar();
-          if (part == 0) {
-            const int key = t * kTileRows + row;
-            float tot = 0.f;
+            float mx[11];
 #pragma unroll
-            for (int p2 = 0; p2 < kParts; ++p2) tot += mg[p2 * 128 + row];
-            if (key < a.N) a.colsum[(size_t)unit * a.N + key] = tot;
-          }
-          acc[0] = acc[1] = acc[2] = acc[3] = 0;
+            for (int i = 0; i < 10; ++i)
+              mx[i] = fm::max3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
+                               __uint_as_float(v[3 * i + 2]));
+            mx[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+            const float cm = fmaxf(fm::max3(fm::max3(mx[0], mx[1], mx[2]), fm::max3(mx[3], mx[4], mx[5]),
+                                            fm::max3(mx[6], mx[7], mx[8])),
+                                   fmaxf(mx[9], mx[10]));
+            // stale running max: rescale only when the group max exceeds it by
+            // more than 8 (log2 units), so the exps need not wait for the max
+            const float cms = cm * sl2;
+            if (cms > m + 8.0f) {
+              l = l * fm::ex2_mufu(m - cms);
+              m = cms;
+            }
+            if (m == -INFINITY) return;
+            const uint64_t nmn = fm::splat2(-m);
+            uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int pr = 0; pr < 16; ++pr) {
+              const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
+                                          sl2x2, nmn);
+              const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
+              acc[pr & 3] = fm::add2(acc[pr & 3], e);
+            }
+            const uint64_t s2 = fm::add2(fm::add2(acc[0], acc[1]), fm::add2(acc[2], acc[3]));
+            float s0, s1;
+            fm::unpack2(s2, s0, s1);
+            l += s0 + s1;
+          });
         }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
       }
-      if (ng_next > 0) ptx::tmem_wait_ld(ra);
+      float* mg = mrg + (t & 1) * (kParts * 256);
+      mg[part * 256 + row * 2] = m;
+      mg[part * 256 + row * 2 + 1] = l;
+      softmax_bar();
+      if (part == 0) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) M = fmaxf(M, mg[p2 * 256 + row * 2]);
+        float L = 0.f;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) {
+          const float mp = mg[p2 * 256 + row * 2];
+          if (mp != -INFINITY) L += mg[p2 * 256 + row * 2 + 1] * fm::ex2_mufu(mp - M);
+        }
+        const int qi = t * kTileRows + row;
+        // stored negated: pass 2 adds it with one packed FMA; padded queries
+        // get -inf and contribute nothing
+        nlse2[qi] = qi < a.N ? -(M + __log2f(L)) : -INFINITY;
+      }
+    }
+    softmax_bar();
+    // pass 2: column sums of exp2(z - lse), one key per TMEM lane
+    for (int t = 0; t < a.nt; ++t) {
+      const bool live = t * kTileRows + quarter * 32 < a.N;
+      uint64_t acc[4] = {0, 0, 0, 0};
+      for (int c = 0; c < a.nchunks; ++c, ++u) {
+        const uint32_t buf = u & 1;
+        wait_bar(&sh.bar_full[buf], (u >> 1) & 1, sh);
+        ptx::tc_fence_after();
+        const int nc = min(kChunkCols, a.Np - kChunkCols * c);
+        const int col0 = part * kPartCols;
+        const int ncols = live ? max(0, min(kPartCols, nc - col0)) : 0;
+        {
+          const uint32_t ta = tbase + lane_addr + buf * kChunkCols + col0;
+          for_groups(ta, ncols >> 5, [&](const uint32_t* v, int g) {
+            const uint64_t* nl = reinterpret_cast<const uint64_t*>(nlse2 + kChunkCols * c + col0 + g);
+#pragma unroll
+            for (int pr = 0; pr < 16; ++pr) {
+              const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
+                                          sl2x2, nl[pr]);
+              const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
+              acc[pr & 3] = fm::add2(acc[pr & 3], e);
+            }
+          });
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
+      }
+      const uint64_t s2 = fm::add2(fm::add2(acc[0], acc[1]), fm::add2(acc[2], acc[3]));
+      float s0, s1;
+      fm::unpack2(s2, s0, s1);
+      float* mg = mrg + (t & 1) * (kParts * 128);
+      mg[part * 128 + row] = s0 + s1;
+      softmax_bar();
+      if (part == 0) {
+        const int key = t * kTileRows + row;
+        float tot = 0.f;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) tot += mg[p2 * 128 + row];
+        if (key < a.N) a.colsum[(size_t)unit * a.N + key] = tot;
+      }
     }
   }
   __syncthreads();
