@@ -49,7 +49,9 @@ def parse():
     p.add_argument("--impl", default="sv", choices=["sv", "reference"])
     p.add_argument("--batch", type=int, default=16)
     p.add_argument("--keep", type=float, default=0.5)
-    p.add_argument("--layers", type=int, default=32)
+    p.add_argument("--layers", type=int, default=None, help="default: the model's layer count")
+    p.add_argument("--workload", default="llava", choices=["llava", "longvila"],
+                   help="decode shape: LLaVA-NeXT-7B (default, the bench line) or LongVILA-7B")
     p.add_argument("--salience-batch", type=int, default=256)
     p.add_argument("--no-salience", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -331,8 +333,12 @@ def main():
     a = parse()
     rank, world, local = dist_env()
     from visual_token_sparsity_gb300 import synth
-    shape = synth.llava_next_decode(batch=a.batch, keep=a.keep, layers=a.layers)
-    config = {"workload": f"{shape.name}: {shape.layers} layers, batch {shape.batch}, {shape.H} MHA heads, d {shape.d}, "
+    if a.workload == "llava":
+        shape = synth.llava_next_decode(batch=a.batch, keep=a.keep, layers=a.layers or 32)
+    else:
+        shape = synth.longvila_decode(batch=a.batch, layers=a.layers or 28)
+    config = {"workload": f"{shape.name}: {shape.layers} layers, batch {shape.batch}, {shape.H} query heads / "
+                          f"{shape.Hkv} KV heads, d {shape.d}, "
                           f"{shape.n_vis} visual + {shape.n_text} text tokens, page 16, retrieval keep {shape.keep} "
                           f"(k={shape.k}), 1 query row",
               "global_batch": shape.batch * world, "layers": shape.layers, "keep": shape.keep,

@@ -218,7 +218,9 @@ sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const sv_kv_laye
  * out     : out bf16 [B][H][d].
  * lse     : optional out fp32 [B][H], log sum_t exp(scale q.k_t) (NULL = none).
  * Split-K over tokens with an fp32 online softmax; per-split partials live in
- * ws and are merged by a second kernel.  Supported: d in {64, 128}.
+ * ws and are merged in the same kernel (or a second one when there are many
+ * splits).  G <= 2 uses CUDA-core dot products, 3 <= G <= 16 warp-level
+ * tensor-core tiles.  Supported: d in {64, 128}, G = H / Hkv <= 16.
  */
 sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
                                 const sv_seq_batch* seqs, const int32_t* vis_idx, int k,

@@ -228,6 +228,9 @@ def test_retrieve_rows_equal_presummed_row(lib):
     (6, 2, 64, 50, 0, 2, 13, True),         # no text tokens
     (6, 2, 64, 50, 7, 2, 1, True),          # a single visual token
     (5, 5, 64, 40, 9, 3, 40, False),        # every visual token, listed unsorted
+    (16, 1, 64, 300, 17, 2, 77, True),      # 16 heads per KV head (tensor-core tiles, no padding rows)
+    (12, 1, 128, 500, 40, 1, 200, False),   # 12 heads per KV head
+    (28, 4, 128, 50176, 256, 1, 12544, True),  # LongVILA shape, one sequence
 ])
 def test_sparse_attention_matches_oracle(lib, H, Hkv, d, n_vis, n_text, B, k, sort):
     shape = synth.DecodeShape("t", H=H, Hkv=Hkv, d=d, n_vis=n_vis, n_text=n_text, layers=1, batch=B,

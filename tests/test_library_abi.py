@@ -83,9 +83,9 @@ def test_host_validation_rejects_before_launch(so):
     seqs_long = binding.sv_seq_batch(_fake(), 1, 10, 150, 20)
     assert lib.sv_retrieve_topk(_fake(), 1, 4, ctypes.byref(layer), ctypes.byref(seqs_long), 10, _fake(),
                                 None, _fake(), 1 << 20, s) == 1
-    # attention: group size above 8
+    # attention: group size above 16
     layer1 = binding.sv_kv_layer(_fake(), _fake(), 100, 1, 64)
-    assert lib.sv_sparse_decode_attn(_fake(), 16, 0.1, ctypes.byref(layer1), ctypes.byref(seqs), None, 0,
+    assert lib.sv_sparse_decode_attn(_fake(), 17, 0.1, ctypes.byref(layer1), ctypes.byref(seqs), None, 0,
                                      _fake(), None, _fake(), 1 << 20, s) == 2
     # eviction span outside the text
     assert lib.sv_evict_qa_tokens(ctypes.byref(layer), 1, ctypes.byref(seqs), 5, 11, None, _fake(), 256, s) == 1
@@ -97,7 +97,7 @@ def test_workspace_sizes_are_monotone_in_tokens(so):
     lib = binding.load(so)
     for B, H, Hkv, d in ((1, 32, 32, 128), (16, 32, 32, 128), (8, 28, 4, 128), (1, 4, 2, 64)):
         prev = 0
-        for n in range(1, 14000, 97):
+        for n in range(1, 60000, 97):
             w = lib.sv_attn_workspace_bytes(B, H, Hkv, d, n)
             assert w >= prev and w >= 256
             prev = w

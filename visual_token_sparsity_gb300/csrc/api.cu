@@ -168,8 +168,12 @@ sv_status sv_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx
   if (k < 1 || k > n) return fail(SV_ERR_INVALID_ARG, "need 1 <= k <= n (k = %d, n = %d)", k, n);
   sv_status s = check_ws(ws, ws_bytes, sv_topk_workspace_bytes(rows, n, k));
   if (s != SV_OK) return s;
-  return cuda_status(sv::launch_topk_rows(scores, rows, n, k, idx, static_cast<cudaStream_t>(stream)),
-                     "sv_topk_rows");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // long rows: a cluster of CTAs per row; otherwise one CTA per row
+  const cudaError_t e = (n > 16384 && sv::topk_cluster_fits(n))
+                            ? sv::launch_topk_cluster(scores, rows, n, k, idx, st)
+                            : sv::launch_topk_rows(scores, rows, n, k, idx, st);
+  return cuda_status(e, "sv_topk_rows");
 }
 
 sv_status sv_prune_compact(const float* salience, int B, int N, int k, const void* feat,
@@ -226,7 +230,7 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
   if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q must be 16-byte aligned");
   const int Hkv = layer->n_kv_heads;
   if (H <= 0 || H % Hkv) return fail(SV_ERR_INVALID_ARG, "H must be a positive multiple of n_kv_heads");
-  if (H / Hkv > 8) return fail(SV_ERR_UNSUPPORTED, "query heads per KV head %d > 8", H / Hkv);
+  if (H / Hkv > 16) return fail(SV_ERR_UNSUPPORTED, "query heads per KV head %d > 16", H / Hkv);
   if (!std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale must be finite");
   const int k_vis = vis_idx ? k : seqs->n_vis;
   if (vis_idx && (k < 0 || k > seqs->n_vis)) return fail(SV_ERR_INVALID_ARG, "need 0 <= k <= n_vis");

@@ -8,6 +8,9 @@
 //   out = sum_{t in T} softmax_t(scale q.k_t) v_t
 // with an fp32 online softmax in the log2 domain.
 //
+// This file holds the CUDA-core kernel used for G <= 2 query heads per KV
+// head; attn_mma.cu holds the tensor-core kernel for larger groups.
+//
 // Split-K: every warp owns one (sequence, KV head, token split) and streams
 // its tokens in tiles.  Per tile each lane looks up one token's page through
 // the block table, the warp issues all K and V row loads (16 B per lane, whole
@@ -19,6 +22,13 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#ifndef SV_ATTN_TILE
+#define SV_ATTN_TILE 32        // tokens per warp step of the G <= 2 kernel
+#endif
+#ifndef SV_ATTN_MIN_BLOCKS
+#define SV_ATTN_MIN_BLOCKS 3   // resident CTAs per SM the G = 1 kernel is register-capped for
+#endif
+
 namespace sv {
 
 namespace {
@@ -27,7 +37,7 @@ template <int D, int G>
 struct AttnShape {
   static constexpr int LPT = D / 8;
   static constexpr int TPI = 32 / LPT;
-  static constexpr int TILE = G <= 2 ? 32 : (G <= 4 ? 16 : 8);
+  static constexpr int TILE = G <= 2 ? SV_ATTN_TILE : (G <= 4 ? 16 : 8);
   static constexpr int NL = TILE / TPI;
   static constexpr int DUP = LPT / NL;
 };
@@ -35,9 +45,12 @@ struct AttnShape {
 constexpr int kAttnWarps = 4;
 constexpr int kAttnTargetWarps = 4096;
 constexpr int kAttnMaxSplits = 1024;
+constexpr int kFusedMergeMaxSplits = 32;   // above this a separate merge kernel runs
 constexpr uint32_t kNoRow = 0xffffffffu;
 
-int attn_tile(int G) { return G <= 2 ? 32 : (G <= 4 ? 16 : 8); }
+// tokens per warp step: 32 for the CUDA-core kernel (G <= 2), one 16-token
+// MMA sub-tile for the tensor-core kernel (attn_mma.cu, G >= 3)
+int attn_tile(int G) { return G <= 2 ? SV_ATTN_TILE : 16; }
 
 }  // namespace
 
@@ -51,11 +64,18 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   if (tpw < 1) tpw = 1;
   long long min_tpw = (tiles + kAttnMaxSplits - 1) / kAttnMaxSplits;
   if (tpw < min_tpw) tpw = min_tpw;
+  // small tiles (large G): at least 128 tokens per split, or the partials
+  // (G x (d + 2) floats per split) and their merge dominate
+  const long long min_tokens = G > 2 ? 128 : 0;
+  if (tpw * p.tile < min_tokens) tpw = (min_tokens + p.tile - 1) / p.tile;
   p.chunk = (int)(tpw * p.tile);
   p.nsplit = n_tokens > 0 ? (n_tokens + p.chunk - 1) / p.chunk : 1;
   // nsplit <= ceil(tiles / tpw) <= min(tiles, ceil(target / units), max): a
   // bound that never decreases as n_tokens grows (workspace sizing).
-  long long ub = tiles > 0 ? tiles : 1;
+  // chunk >= max(tile, min_tokens), so nsplit <= ceil(n_tokens / that)
+  const long long min_chunk = min_tokens > p.tile ? (min_tokens + p.tile - 1) / p.tile * p.tile : p.tile;
+  long long ub = (n_tokens + min_chunk - 1) / min_chunk;
+  if (ub < 1) ub = 1;
   const long long per_unit = (kAttnTargetWarps + units - 1) / (units > 0 ? units : 1);
   if (ub > per_unit) ub = per_unit;
   if (ub > kAttnMaxSplits) ub = kAttnMaxSplits;
@@ -64,7 +84,7 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32, (G == 1 ? 3 : 1))
+__global__ void __launch_bounds__(kAttnWarps * 32, (G == 1 ? SV_ATTN_MIN_BLOCKS : 1))
 sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
                          const uint16_t* __restrict__ k_pool, const uint16_t* __restrict__ v_pool,
                          int num_blocks, int Hkv, const int32_t* __restrict__ block_table,
@@ -112,26 +132,30 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   const int my_slot = (lane % LPT) / DUP;              // value index after the fold
   const int my_tok = my_slot * TPI + lane / LPT;       // token of the tile held after the fold
 
-  for (int t0 = t_begin; t0 < t_end; t0 += TILE) {
-    uint32_t rowid = kNoRow;
+  // Token -> pool row id for the TILE tokens starting at t0 (lane < TILE), as
+  // a 2-stage software pipeline: a tile's visual indices are loaded two tiles
+  // ahead and its page-table entries one tile ahead, so no load's latency
+  // falls inside the iteration that needs it.
+  auto load_pos = [&](int t0) -> int {
     const int tok = t0 + lane;
-    if (lane < TILE && tok < t_end) {
-      int pos;
-      if (tok < k_vis) {
-        pos = vrow ? __ldg(vrow + tok) : tok;
-        if (pos < 0 || pos >= n_vis) { flag_status(status, kStatusBadIndex); pos = -1; }
-      } else {
-        pos = n_vis + (tok - k_vis);
-      }
-      if (pos >= 0) {
-        const int page = __ldg(bt + (pos >> 4));
-        if (page >= 0 && page < num_blocks)
-          rowid = (((uint32_t)page * (uint32_t)Hkv + (uint32_t)g) << 4) | (uint32_t)(pos & 15);
-        else
-          flag_status(status, kStatusBadBlock);
-      }
-    }
-
+    if (lane >= TILE || tok >= t_end) return -1;
+    if (tok >= k_vis) return n_vis + (tok - k_vis);
+    const int pos = vrow ? __ldg(vrow + tok) : tok;
+    if (pos < 0 || pos >= n_vis) { flag_status(status, kStatusBadIndex); return -1; }
+    return pos;
+  };
+  auto lookup = [&](int pos) -> uint32_t {
+    if (pos < 0) return kNoRow;
+    const int page = __ldg(bt + (pos >> 4));
+    if (page >= 0 && page < num_blocks)
+      return (((uint32_t)page * (uint32_t)Hkv + (uint32_t)g) << 4) | (uint32_t)(pos & 15);
+    flag_status(status, kStatusBadBlock);
+    return kNoRow;
+  };
+  uint32_t next_rowid = lookup(load_pos(t_begin));
+  int pos_ahead = load_pos(t_begin + TILE);
+  for (int t0 = t_begin; t0 < t_end; t0 += TILE) {
+    const uint32_t rowid = next_rowid;
     uint4 kd[NL], vd[NL];
 #pragma unroll
     for (int i = 0; i < NL; ++i) {
@@ -145,6 +169,8 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
       }
     }
     const bool mine_valid = __shfl_sync(0xffffffffu, rowid, my_tok) != kNoRow;
+    next_rowid = lookup(pos_ahead);
+    pos_ahead = load_pos(t0 + 2 * TILE);
 
     float p[G];
 #pragma unroll
@@ -223,6 +249,8 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
 
   // The last warp to finish this (sequence, KV head) merges every split:
   // out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, M = max_s m_s.
+  // (With many splits a separate merge kernel does this instead.)
+  if (split_done == nullptr) return;
   __threadfence();
   __syncwarp();
   int last = 0;
@@ -274,21 +302,76 @@ static bool dispatch_g(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
   switch (a.H / a.Hkv) {
     case 1: launch_split<D, 1>(a, p, s); return true;
     case 2: launch_split<D, 2>(a, p, s); return true;
-    case 3: launch_split<D, 3>(a, p, s); return true;
-    case 4: launch_split<D, 4>(a, p, s); return true;
-    case 5: launch_split<D, 5>(a, p, s); return true;
-    case 6: launch_split<D, 6>(a, p, s); return true;
-    case 7: launch_split<D, 7>(a, p, s); return true;
-    case 8: launch_split<D, 8>(a, p, s); return true;
     default: return false;
   }
+}
+
+// Merges the per-split partials of one (sequence, query head) when there are
+// too many splits for the fused single-warp merge: split weights are staged
+// in shared memory, then every thread (one output dim) sums the weighted
+// partials with 8 independent accumulators so 8 loads are in flight.
+__global__ void __launch_bounds__(128)
+attn_merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o, int H, int Hkv,
+                  int G, int D, int nsplit, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  extern __shared__ float wsh[];   // nsplit weights
+  __shared__ float red[4];
+  const int bh = blockIdx.x;
+  const int b = bh / H, h = bh % H;
+  const int g = h / G, hh = h % G;
+  const size_t base = ((size_t)b * Hkv + g) * nsplit;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float mx = -INFINITY;
+  for (int s = tid; s < nsplit; s += blockDim.x) mx = fmaxf(mx, part_ml[((base + s) * G + hh) * 2]);
+  mx = warp_max(mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  float lacc = 0.f;
+  for (int s = tid; s < nsplit; s += blockDim.x) {
+    const float ms = part_ml[((base + s) * G + hh) * 2];
+    const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
+    wsh[s] = w;
+    lacc = fmaf(w, part_ml[((base + s) * G + hh) * 2 + 1], lacc);
+  }
+  lacc = warp_sum(lacc);
+  if (lane == 0) red[warp] = lacc;
+  __syncthreads();
+  const float L = (red[0] + red[1]) + (red[2] + red[3]);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const size_t stride = (size_t)G * D;
+  for (int e = tid; e < D; e += blockDim.x) {
+    const float* po = part_o + (base * G + hh) * D + e;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int s = 0;
+    for (; s + 8 <= nsplit; s += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = fmaf(wsh[s + u], po[(size_t)(s + u) * stride], a[u]);
+    }
+    for (; s < nsplit; ++s) a[0] = fmaf(wsh[s], po[(size_t)s * stride], a[0]);
+    const float v = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    out[(size_t)bh * D + e] = (uint16_t)f32_to_bf16_bits(v * inv);
+  }
+  if (lse != nullptr && tid == 0) lse[bh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.H / a.Hkv;
   const AttnPlan p = attn_plan(a.batch, a.Hkv, G, a.k_vis + a.n_text);
-  const bool ok = a.D == 128 ? dispatch_g<128>(a, p, stream) : dispatch_g<64>(a, p, stream);
-  if (!ok) return cudaErrorInvalidValue;
+  AttnArgs b = a;
+  const bool fused_merge = p.nsplit <= kFusedMergeMaxSplits;
+  if (!fused_merge) b.split_done = nullptr;
+  cudaError_t e;
+  if (G >= 3) {
+    e = launch_sparse_attn_mma(b, p, stream);
+  } else {
+    const bool ok = a.D == 128 ? dispatch_g<128>(b, p, stream) : dispatch_g<64>(b, p, stream);
+    if (!ok) return cudaErrorInvalidValue;
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess || fused_merge) return e;
+  attn_merge_kernel<<<a.batch * a.H, 128, (size_t)p.nsplit * sizeof(float), stream>>>(
+      a.part_ml, a.part_o, a.H, a.Hkv, G, a.D, p.nsplit, static_cast<uint16_t*>(a.out), a.lse);
   return cudaGetLastError();
 }
 }  // namespace sv

@@ -15,9 +15,13 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
                             int batch, float* scores, int* status, int num_sms, int* row_done, int k,
                             int32_t* vis_idx, cudaStream_t stream);
 
-// ---- row top-k (topk.cu)
+// ---- row top-k (topk.cu: one CTA per row; topk_cluster.cu: an 8-CTA cluster
+// per row for long rows)
 cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
                              cudaStream_t stream);
+bool topk_cluster_fits(int n);
+cudaError_t launch_topk_cluster(const float* scores, int rows, int n, int k, int32_t* idx,
+                                cudaStream_t stream);
 
 // ---- sparse decode attention (attn.cu)
 struct AttnPlan {
@@ -47,6 +51,7 @@ struct AttnArgs {
   int* status;
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_sparse_attn_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 
 // ---- compaction gather (prune.cu)
 cudaError_t launch_gather_rows(const void* feat, int B, int N, int k, int64_t row_bytes,

@@ -25,6 +25,14 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
 }
 
+// Histogram increment aggregated over the lanes of a warp that hit the same
+// bin (the leading digit of similar-magnitude floats falls into few bins, and
+// same-address shared atomics serialise).  bin < 0 adds nothing.
+__device__ __forceinline__ void hist_add(int* hist, int bin) {
+  const unsigned peers = __match_any_sync(__activemask(), bin);
+  if (bin >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
 // Block-wide exclusive scan of one int per thread (blockDim.x a multiple of
 // 32, at most 1024).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tmp) {
@@ -75,7 +83,7 @@ __device__ __forceinline__ void block_topk_row(const float* src, int n, int k, i
     __syncthreads();
     for (int i = tid; i < n; i += nt) {
       const uint32_t key = key_at(i);
-      if ((key & pmask) == prefix) atomicAdd(&ts.hist[(key >> shift) & 255u], 1);
+      hist_add(ts.hist, (key & pmask) == prefix ? (int)((key >> shift) & 255u) : -1);
     }
     __syncthreads();
     if (tid < 32) {
