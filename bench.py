@@ -131,6 +131,27 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload
 
+def aggregate_replicas(per_rank_ms, bytes_per_rank, world, all_reduce_max=None):
+    """Whole-job figure for N independent replicas: each rank processed
+    bytes_per_rank; the job time is the slowest rank's.  all_reduce_max
+    (a callable list -> list, e.g. a torch.distributed MAX all-reduce) is
+    applied to the per-rank times when world > 1.  Returns (ms, GB/s)."""
+    ms = list(per_rank_ms)
+    if world > 1 and all_reduce_max is not None:
+        ms = all_reduce_max(ms)
+    return ms, world * bytes_per_rank / (ms[0] * 1e-3) / 1e9
+
+
+def torch_max_reducer(device):
+    import torch.distributed as dist
+
+    def red(vals):
+        t = torch.tensor(vals, dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.tolist()
+    return red
+
+
 def decode_bytes(shape):
     """Algorithmic HBM bytes of one decode step (all layers, whole batch)."""
     d2 = shape.d * 2
@@ -415,12 +436,8 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
     with ClockSampler(torch.cuda.current_device()) as clk:
         ms = replay_timed(g_step, a.steps, stream, barrier)
     ms_attn = replay_timed(g_attn, a.steps, stream, barrier)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, ms_attn], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_attn = t.tolist()
-    value = world * bytes_step / (ms * 1e-3) / 1e9
+    (ms, ms_attn), value = aggregate_replicas([ms, ms_attn], bytes_step, world,
+                                              torch_max_reducer(dev) if world > 1 else None)
 
     t_ret, t_att = per_call_times(wl, max(3, a.steps // 4), stream)
     per_launch_ret = rb / (shape.layers)

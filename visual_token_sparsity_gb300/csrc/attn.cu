@@ -307,14 +307,16 @@ static bool dispatch_g(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
 }
 
 // Merges the per-split partials of one (sequence, query head) when there are
-// too many splits for the fused single-warp merge: split weights are staged
-// in shared memory, then every thread (one output dim) sums the weighted
-// partials with 8 independent accumulators so 8 loads are in flight.
-__global__ void __launch_bounds__(128)
+// too many splits for the fused single-warp merge.  256 threads: the split
+// weights 2^(m_s - M) go to shared memory, then each of the 8 warps sums every
+// 8th split (lanes over output dims, 4 splits' loads in flight per lane) and
+// the 8 partial vectors are added in shared memory.
+__global__ void __launch_bounds__(256)
 attn_merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o, int H, int Hkv,
                   int G, int D, int nsplit, uint16_t* __restrict__ out, float* __restrict__ lse) {
   extern __shared__ float wsh[];   // nsplit weights
-  __shared__ float red[4];
+  __shared__ float red[8];
+  __shared__ float4 part[8][32];
   const int bh = blockIdx.x;
   const int b = bh / H, h = bh % H;
   const int g = h / G, hh = h % G;
@@ -325,7 +327,8 @@ attn_merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ p
   mx = warp_max(mx);
   if (lane == 0) red[warp] = mx;
   __syncthreads();
-  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float M = red[0];
+  for (int i = 1; i < 8; ++i) M = fmaxf(M, red[i]);
   __syncthreads();
   float lacc = 0.f;
   for (int s = tid; s < nsplit; s += blockDim.x) {
@@ -337,20 +340,42 @@ attn_merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ p
   lacc = warp_sum(lacc);
   if (lane == 0) red[warp] = lacc;
   __syncthreads();
-  const float L = (red[0] + red[1]) + (red[2] + red[3]);
+  float L = 0.f;
+  for (int i = 0; i < 8; ++i) L += red[i];
   const float inv = L > 0.f ? 1.f / L : 0.f;
+  // lanes cover the output dims 4 at a time (D = 128: 32 lanes; D = 64: 16 lanes)
+  const int nl = D / 4;
   const size_t stride = (size_t)G * D;
-  for (int e = tid; e < D; e += blockDim.x) {
-    const float* po = part_o + (base * G + hh) * D + e;
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int s = 0;
-    for (; s + 8 <= nsplit; s += 8) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) a[u] = fmaf(wsh[s + u], po[(size_t)(s + u) * stride], a[u]);
+  const float* po = part_o + (base * G + hh) * D + lane * 4;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  if (lane < nl) {
+    int s = warp;
+    for (; s + 8 < nsplit; s += 16) {
+      const float4 x0 = *reinterpret_cast<const float4*>(po + (size_t)s * stride);
+      const float4 x1 = *reinterpret_cast<const float4*>(po + (size_t)(s + 8) * stride);
+      const float w0 = wsh[s], w1 = wsh[s + 8];
+      a0.x = fmaf(w0, x0.x, a0.x); a0.y = fmaf(w0, x0.y, a0.y); a0.z = fmaf(w0, x0.z, a0.z); a0.w = fmaf(w0, x0.w, a0.w);
+      a1.x = fmaf(w1, x1.x, a1.x); a1.y = fmaf(w1, x1.y, a1.y); a1.z = fmaf(w1, x1.z, a1.z); a1.w = fmaf(w1, x1.w, a1.w);
     }
-    for (; s < nsplit; ++s) a[0] = fmaf(wsh[s], po[(size_t)s * stride], a[0]);
-    const float v = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-    out[(size_t)bh * D + e] = (uint16_t)f32_to_bf16_bits(v * inv);
+    for (; s < nsplit; s += 8) {
+      const float4 x0 = *reinterpret_cast<const float4*>(po + (size_t)s * stride);
+      const float w0 = wsh[s];
+      a0.x = fmaf(w0, x0.x, a0.x); a0.y = fmaf(w0, x0.y, a0.y); a0.z = fmaf(w0, x0.z, a0.z); a0.w = fmaf(w0, x0.w, a0.w);
+    }
+  }
+  part[warp][lane] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+  __syncthreads();
+  if (warp == 0 && lane < nl) {
+    float4 t = part[0][lane];
+    for (int i = 1; i < 8; ++i) {
+      const float4 u = part[i][lane];
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
+    uint16_t* dst = out + (size_t)bh * D + lane * 4;
+    dst[0] = (uint16_t)f32_to_bf16_bits(t.x * inv);
+    dst[1] = (uint16_t)f32_to_bf16_bits(t.y * inv);
+    dst[2] = (uint16_t)f32_to_bf16_bits(t.z * inv);
+    dst[3] = (uint16_t)f32_to_bf16_bits(t.w * inv);
   }
   if (lse != nullptr && tid == 0) lse[bh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
@@ -370,7 +395,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
   }
   if (e != cudaSuccess || fused_merge) return e;
-  attn_merge_kernel<<<a.batch * a.H, 128, (size_t)p.nsplit * sizeof(float), stream>>>(
+  attn_merge_kernel<<<a.batch * a.H, 256, (size_t)p.nsplit * sizeof(float), stream>>>(
       a.part_ml, a.part_o, a.H, a.Hkv, G, a.D, p.nsplit, static_cast<uint16_t*>(a.out), a.lse);
   return cudaGetLastError();
 }

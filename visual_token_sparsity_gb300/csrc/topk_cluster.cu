@@ -7,7 +7,8 @@
 // order-preserving keys in its shared memory.  Each of the four radix passes
 // builds a local 256-bin histogram, and after a cluster barrier every CTA
 // sums the cluster's histograms through distributed shared memory and picks
-// the same digit.  The output phase exchanges per-CTA (greater, equal) counts
+// the same digit (histograms are double-buffered, so one cluster barrier per
+// pass is enough).  The output phase exchanges per-CTA (greater, equal) counts
 // the same way, so the CTAs write disjoint ranges of the ascending index list,
 // with ties broken towards the lower index exactly as in the single-CTA
 // routine (topk_block.cuh).  The cluster barriers are hardware barriers over
@@ -30,7 +31,7 @@ constexpr int kTopkClusterThreads = 512;
 __global__ void __cluster_dims__(kTopkClusterCtas, 1, 1) __launch_bounds__(kTopkClusterThreads)
 topk_cluster_kernel(const float* __restrict__ scores, int n, int k, int32_t* __restrict__ idx) {
   extern __shared__ uint32_t keys[];
-  __shared__ int hist[256];
+  __shared__ int hist[2][256];    // double-buffered: peers read pass p's while pass p+1 fills the other
   __shared__ int total[256];
   __shared__ int scan_tmp[33];
   __shared__ int sel_digit, sel_above;
@@ -51,16 +52,18 @@ topk_cluster_kernel(const float* __restrict__ scores, int n, int k, int32_t* __r
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += nt) hist[i] = 0;
+    int* hcur = hist[pass & 1];
+    for (int i = tid; i < 256; i += nt) hcur[i] = 0;
     __syncthreads();
     for (int i = tid; i < m; i += nt) {
       const uint32_t key = keys[i];
-      hist_add(hist, (key & pmask) == prefix ? (int)((key >> shift) & 255u) : -1);
+      hist_add(hcur, (key & pmask) == prefix ? (int)((key >> shift) & 255u) : -1);
     }
     cluster.sync();                                   // all local histograms complete
     for (int b = tid; b < 256; b += nt) {
       int s = 0;
-      for (int r = 0; r < kTopkClusterCtas; ++r) s += cluster.map_shared_rank(hist, r)[b];
+#pragma unroll
+      for (int r = 0; r < kTopkClusterCtas; ++r) s += cluster.map_shared_rank(hcur, r)[b];
       total[b] = s;
     }
     __syncthreads();
@@ -88,7 +91,7 @@ topk_cluster_kernel(const float* __restrict__ scores, int n, int k, int32_t* __r
     prefix |= (uint32_t)sel_digit << shift;
     pmask |= 255u << shift;
     remaining -= sel_above;
-    cluster.sync();                                   // histograms may be reused
+    __syncthreads();          // total / sel_* are rewritten by the next pass
   }
   const uint32_t T = prefix;
 
