@@ -44,7 +44,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="sv", choices=["sv", "reference"])
     p.add_argument("--batch", type=int, default=16)
@@ -94,7 +94,8 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)      # let the sampler start before the timed region
         except Exception:
             self.proc = None
         return self
@@ -410,7 +411,7 @@ def main():
     if not a.no_decode:
         decode_measure(a, shape, dev, stream, barrier, world, pk, line)
     if not a.no_salience:
-        ss, sms, flops = salience_measure(a.salience_batch, max(3, a.steps // 2), 3, stream)
+        ss, sms, flops = salience_measure(a.salience_batch, min(50, max(3, a.steps // 2)), 3, stream)
         tf = flops / (sms * 1e-3) / 1e12
         line["salience"] = {"workload": f"{ss.name}: {ss.batch} frames x {ss.N} tokens, {ss.H} heads, d {ss.d}",
                             "ms": sms, "tokens_per_s": ss.batch * ss.N / (sms * 1e-3),
@@ -439,7 +440,7 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
     (ms, ms_attn), value = aggregate_replicas([ms, ms_attn], bytes_step, world,
                                               torch_max_reducer(dev) if world > 1 else None)
 
-    t_ret, t_att = per_call_times(wl, max(3, a.steps // 4), stream)
+    t_ret, t_att = per_call_times(wl, min(20, max(3, a.steps // 4)), stream)
     per_launch_ret = rb / (shape.layers)
     per_launch_att = ab / (shape.layers)
     if t_att >= t_ret:
@@ -461,7 +462,7 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
             "hbm_frac_step": (bytes_step / (ms * 1e-3) / 1e9) / pk["hbm_gbs"]})
 
     if not a.no_e2e:
-        e2e, h2d, d2h = e2e_throughput(wl, max(3, a.steps // 2), 2, stream, bytes_step)
+        e2e, h2d, d2h = e2e_throughput(wl, min(50, max(3, a.steps // 2)), 2, stream, bytes_step)
         line["e2e"] = {"value": world * e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     del wl, g_step, g_attn
     torch.cuda.empty_cache()

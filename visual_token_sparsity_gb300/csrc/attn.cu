@@ -25,6 +25,9 @@
 #ifndef SV_ATTN_TILE
 #define SV_ATTN_TILE 32        // tokens per warp step of the G <= 2 kernel
 #endif
+#ifndef SV_ATTN_MMA_MIN_G
+#define SV_ATTN_MMA_MIN_G 3    // groups of at least this many heads use the tensor-core kernel
+#endif
 #ifndef SV_ATTN_MIN_BLOCKS
 #define SV_ATTN_MIN_BLOCKS 3   // resident CTAs per SM the G = 1 kernel is register-capped for
 #endif
@@ -50,7 +53,8 @@ constexpr uint32_t kNoRow = 0xffffffffu;
 
 // tokens per warp step: 32 for the CUDA-core kernel (G <= 2), one 16-token
 // MMA sub-tile for the tensor-core kernel (attn_mma.cu, G >= 3)
-int attn_tile(int G) { return G <= 2 ? SV_ATTN_TILE : 16; }
+bool attn_uses_mma(int G) { return G >= SV_ATTN_MMA_MIN_G; }
+int attn_tile(int G) { return attn_uses_mma(G) ? 16 : SV_ATTN_TILE; }
 
 }  // namespace
 
@@ -66,7 +70,7 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   if (tpw < min_tpw) tpw = min_tpw;
   // small tiles (large G): at least 128 tokens per split, or the partials
   // (G x (d + 2) floats per split) and their merge dominate
-  const long long min_tokens = G > 2 ? 128 : 0;
+  const long long min_tokens = attn_uses_mma(G) ? 128 : 0;
   if (tpw * p.tile < min_tokens) tpw = (min_tokens + p.tile - 1) / p.tile;
   p.chunk = (int)(tpw * p.tile);
   p.nsplit = n_tokens > 0 ? (n_tokens + p.chunk - 1) / p.chunk : 1;
@@ -387,7 +391,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const bool fused_merge = p.nsplit <= kFusedMergeMaxSplits;
   if (!fused_merge) b.split_done = nullptr;
   cudaError_t e;
-  if (G >= 3) {
+  if (attn_uses_mma(G)) {
     e = launch_sparse_attn_mma(b, p, stream);
   } else {
     const bool ok = a.D == 128 ? dispatch_g<128>(b, p, stream) : dispatch_g<64>(b, p, stream);

@@ -62,22 +62,6 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
 
-  // q_bar = sum over query rows r and the group's heads, fp32, fixed order.
-  for (int e = tid; e < D; e += blockDim.x) {
-    float acc = 0.f;
-    for (int r = 0; r < R; ++r) {
-      const uint16_t* qr = q + (((size_t)b * R + r) * H + (size_t)g * G) * D + e;
-      for (int hh = 0; hh < G; ++hh) acc += __uint_as_float((uint32_t)qr[(size_t)hh * D] << 16);
-    }
-    qbar[e] = acc;
-  }
-  __syncthreads();
-
-  float qv[8];
-  const int dim0 = (lane % LPT) * 8;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) qv[e] = qbar[dim0 + e];
-
   const int n_vblocks = (n_vis + kBlockTokens - 1) / kBlockTokens;
   const int blk_begin = blockIdx.x * blocks_per_cta;
   const int blk_end = min(n_vblocks, blk_begin + blocks_per_cta);
@@ -96,12 +80,32 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
       kv[i] = ok ? ld_stream16(base + (size_t)(lane + 32 * i) * 8) : make_uint4(0, 0, 0, 0);
   };
 
+  // the first page's loads are issued before the q_bar prologue so that its
+  // latency overlaps the prologue's loads and barrier
   uint4 cur[NL], nxt[NL];
-  int blk = blk_begin + warp;
-  if (SV_RET_PREFETCH && blk < blk_end) load_page(blk, cur);
+  const int blk0 = blk_begin + warp;
+  if (blk0 < blk_end) load_page(blk0, cur);
+
+  // q_bar = sum over query rows r and the group's heads, fp32, fixed order.
+  for (int e = tid; e < D; e += blockDim.x) {
+    float acc = 0.f;
+    for (int r = 0; r < R; ++r) {
+      const uint16_t* qr = q + (((size_t)b * R + r) * H + (size_t)g * G) * D + e;
+      for (int hh = 0; hh < G; ++hh) acc += __uint_as_float((uint32_t)qr[(size_t)hh * D] << 16);
+    }
+    qbar[e] = acc;
+  }
+  __syncthreads();
+
+  float qv[8];
+  const int dim0 = (lane % LPT) * 8;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) qv[e] = qbar[dim0 + e];
+
+  int blk = blk0;
   for (; blk < blk_end; blk += nwarps) {
-    if (!SV_RET_PREFETCH) load_page(blk, cur);
-    else if (blk + nwarps < blk_end) load_page(blk + nwarps, nxt);
+    if (!SV_RET_PREFETCH && blk != blk0) load_page(blk, cur);
+    else if (SV_RET_PREFETCH && blk + nwarps < blk_end) load_page(blk + nwarps, nxt);
     float part[NL];
 #pragma unroll
     for (int i = 0; i < NL; ++i) {
