@@ -132,6 +132,22 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload
 
+def measured_traffic(call):
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)
+    recorded in profiles/traffic.json for this C call, or None when the
+    kernel source has changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))[call]
+        src = os.path.join(ROOT, rec["source"])
+        if hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
+            return None
+        return rec["bytes_per_launch"]
+    except Exception:
+        return None
+
+
 def aggregate_replicas(per_rank_ms, bytes_per_rank, world, all_reduce_max=None):
     """Whole-job figure for N independent replicas: each rank processed
     bytes_per_rank; the job time is the slowest rank's.  all_reduce_max
@@ -444,9 +460,9 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
     per_launch_ret = rb / (shape.layers)
     per_launch_att = ab / (shape.layers)
     if t_att >= t_ret:
-        dom = ("sv_sparse_decode_attn (split-K gather attention + combine)", per_launch_att, t_att)
+        dom = ("sv_sparse_decode_attn (split-K gather attention + combine)", per_launch_att, t_att, "attention")
     else:
-        dom = ("sv_retrieve_topk (paged GEMV + radix top-k)", per_launch_ret, t_ret)
+        dom = ("sv_retrieve_topk (paged GEMV + radix top-k)", per_launch_ret, t_ret, "retrieve")
     achieved = dom[1] / (dom[2] * 1e-3) / 1e9
 
     line.update({"value": value, "ms_per_step": ms, "decode_step_us": ms * 1e3,
@@ -457,7 +473,9 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
             "gpu_launches": a.steps * shape.layers * ((1 if shape.n_vis <= 11264 else 2) + 1),
             "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
-                         "traffic": None,
+                         "traffic": (measured_traffic(f"{dom[3]}:{shape.name}:b{shape.batch}:keep{shape.keep}")
+                                     if world == 1 else None),
+                         "algorithmic_bytes_per_launch": dom[1],
                          "per_call_us": {"retrieve": t_ret * 1e3, "attention": t_att * 1e3}},
             "hbm_frac_step": (bytes_step / (ms * 1e-3) / 1e9) / pk["hbm_gbs"]})
 
