@@ -47,11 +47,12 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="sv", choices=["sv", "reference"])
-    p.add_argument("--batch", type=int, default=16)
+    p.add_argument("--batch", type=int, default=None, help="default: 16 (llava), 8 (longvila), 1 (tiny, rounds)")
     p.add_argument("--keep", type=float, default=0.5)
     p.add_argument("--layers", type=int, default=None, help="default: the model's layer count")
-    p.add_argument("--workload", default="llava", choices=["llava", "longvila"],
-                   help="decode shape: LLaVA-NeXT-7B (default, the bench line) or LongVILA-7B")
+    p.add_argument("--workload", default="llava", choices=["llava", "longvila", "tiny", "rounds"],
+                   help="decode shape: LLaVA-NeXT-7B (default, the bench line), LongVILA-7B, the tiny "
+                        "single-layer case, or the 5-round question/answer loop on the tiny shapes")
     p.add_argument("--salience-batch", type=int, default=256)
     p.add_argument("--no-salience", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -303,9 +304,9 @@ def e2e_throughput(wl, steps, warmup, stream, bytes_step):
     return bytes_step / dt / 1e9, h2d, d2h
 
 
-def salience_measure(batch, steps, warmup, stream):
+def salience_measure(batch, steps, warmup, stream, tiny=False):
     from visual_token_sparsity_gb300 import binding as sv, synth
-    ss = synth.siglip_salience(batch=batch)
+    ss = synth.tiny_salience(batch=batch) if tiny else synth.siglip_salience(batch=batch)
     q, k, _ = synth.draw_salience(ss, device="cuda")
     sal = torch.empty(ss.batch, ss.N, device="cuda")
     ws = sv.workspace(sv.sv_salience_workspace_bytes(ss.batch, ss.H, ss.N, ss.d))
@@ -365,16 +366,78 @@ def cpu_baseline(shape, budget_s=10.0):
                       f"fp64 numpy, single thread"}
 
 
+def rounds_main(a):
+    """Latency of the 5-round loop on the tiny shapes: per round, evict the
+    previous question/answer, append the 32-token question, retrieve the
+    top-25% visual tokens with its 32 query rows, then 256 decode steps of
+    (append one token, sparse attention).  Every round starts from the same
+    cache state (visual tokens + 32-token prefix), so one CUDA graph of a
+    round is replayed; inputs are seeded device buffers."""
+    from visual_token_sparsity_gb300 import binding as sv, synth
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    s = synth.multiturn(batch=a.batch)
+    dev = torch.device("cuda", 0)
+    bt = synth.random_block_table(s.batch, s.max_blocks, s.num_blocks, seed=synth.subseed(s.seed, 0, 98)).to(dev)
+    lay = synth.draw_decode_layer(s, 0, bt, device=dev)
+    layer = sv.KvLayer(lay.k_pool, lay.v_pool)
+    B, Hkv, H, d = s.batch, s.Hkv, s.H, s.d
+    ws_r = sv.workspace(sv.sv_retrieve_workspace_bytes(B, H, Hkv, d, s.n_vis, s.k), dev)
+    ws_a = sv.workspace(sv.sv_attn_workspace_bytes(B, H, Hkv, d, s.k + 32 + 32 + 256), dev)
+    ws_e = sv.workspace(256, dev)
+    g = lambda t: synth.subseed(s.seed, 100, t)
+    qk = synth.normal_bf16((B, 32, Hkv, d), g(1), device=dev)
+    qv = synth.normal_bf16((B, 32, Hkv, d), g(2), device=dev)
+    rows = synth.normal_bf16((B, 32, H, d), g(3), device=dev)
+    ak = synth.normal_bf16((B, 256, 1, Hkv, d), g(4), device=dev)
+    av = synth.normal_bf16((B, 256, 1, Hkv, d), g(5), device=dev)
+    aq = synth.normal_bf16((256, B, H, d), g(6), device=dev)
+    vis = torch.empty(B, Hkv, s.k, dtype=torch.int32, device=dev)
+    outs = torch.empty(256, B, H, d, dtype=torch.bfloat16, device=dev)
+    scale = 1.0 / math.sqrt(d)
+    ak_steps = [ak[:, t].contiguous() for t in range(256)]
+    av_steps = [av[:, t].contiguous() for t in range(256)]
+
+    def one_round():
+        seqs = sv.SeqBatch(bt, s.n_vis, 32 + 32 + 256)      # state after a previous round
+        sv.sv_evict_qa_tokens([layer], seqs, 32, seqs.n_text, ws_e)
+        sv.sv_kv_append(layer, seqs, qk, qv, ws_e)
+        seqs.n_text += 32
+        sv.sv_retrieve_topk(rows, layer, seqs, s.k, vis, None, ws_r)
+        for t in range(256):
+            sv.sv_kv_append(layer, seqs, ak_steps[t], av_steps[t], ws_e)
+            seqs.n_text += 1
+            sv.sv_sparse_decode_attn(aq[t], scale, layer, seqs, vis, s.k, outs[t], None, ws_a)
+
+    stream = torch.cuda.Stream()
+    graph = time_graph(one_round, a.steps, max(3, a.warmup), stream)
+    ms = replay_timed(graph, a.steps, stream, lambda: None)
+    print(json.dumps({"metric": "multi-turn round latency (tiny shapes)", "value": ms * 1e3, "unit": "us/round",
+                      "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "higher_is_better": False,
+                      "per_decode_step_us": ms * 1e3 / 256, "dtype": "bf16", "data": "synthetic",
+                      "gpu_launches": a.steps * (1 + 1 + 256 * 2),
+                      "config": {"workload": "round loop: evict, append 32-token question, retrieve top-25% "
+                                             "with 32 rows, 256 x (append + sparse attention); 4 q / 2 KV "
+                                             "heads, d 64, 576 visual + 32-token prefix", "batch": s.batch}}))
+
+
 # ---------------------------------------------------------------- main
 
 def main():
     a = parse()
+    if a.batch is None:
+        a.batch = {"llava": 16, "longvila": 8}.get(a.workload, 1)
     rank, world, local = dist_env()
     from visual_token_sparsity_gb300 import synth
     if a.workload == "llava":
         shape = synth.llava_next_decode(batch=a.batch, keep=a.keep, layers=a.layers or 32)
-    else:
+    elif a.workload == "longvila":
         shape = synth.longvila_decode(batch=a.batch, layers=a.layers or 28)
+    elif a.workload == "tiny":
+        shape = synth.tiny_decode(batch=a.batch)
+    else:
+        return rounds_main(a)
     config = {"workload": f"{shape.name}: {shape.layers} layers, batch {shape.batch}, {shape.H} query heads / "
                           f"{shape.Hkv} KV heads, d {shape.d}, "
                           f"{shape.n_vis} visual + {shape.n_text} text tokens, page 16, retrieval keep {shape.keep} "
@@ -427,7 +490,9 @@ def main():
     if not a.no_decode:
         decode_measure(a, shape, dev, stream, barrier, world, pk, line)
     if not a.no_salience:
-        ss, sms, flops = salience_measure(a.salience_batch, min(50, max(3, a.steps // 2)), 3, stream)
+        tiny = a.workload == "tiny"
+        ss, sms, flops = salience_measure(1 if tiny else a.salience_batch, min(50, max(3, a.steps // 2)), 3,
+                                          stream, tiny=tiny)
         tf = flops / (sms * 1e-3) / 1e12
         line["salience"] = {"workload": f"{ss.name}: {ss.batch} frames x {ss.N} tokens, {ss.H} heads, d {ss.d}",
                             "ms": sms, "tokens_per_s": ss.batch * ss.N / (sms * 1e-3),
