@@ -117,7 +117,7 @@ size_t sv_evict_workspace_bytes(void);
  * q, k     : bf16 [B][H][N][d], contiguous.
  * scale    : logit scale (1/sqrt(d) for standard attention); must be > 0.
  * salience : out fp32 [B][N]; each row sums to 1.
- * Supported: d = 64 with N <= 1408, d = 72 with N <= 1024, d = 128 with
+ * Supported: d = 64 with N <= 1280, d = 72 with N <= 1024, d = 128 with
  * N <= 512 (one head's keys or queries stay resident in shared memory);
  * other shapes return SV_ERR_UNSUPPORTED.  Computed with tcgen05
  * tensor-core tiles (bf16 operands, fp32 accumulation) in two passes: row

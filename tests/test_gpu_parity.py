@@ -57,7 +57,8 @@ def test_topk_all_equal_takes_lowest_indices(lib):
 @pytest.mark.parametrize("B,H,N,d,std", [(1, 4, 576, 64, 1.0), (2, 16, 729, 72, 1 / math.sqrt(72)),
                                          (1, 2, 729, 72, 1.0), (3, 1, 1, 64, 1.0), (1, 2, 17, 72, 1.0),
                                          (2, 3, 130, 64, 1.0), (1, 2, 200, 128, 1.0),
-                                         (1, 1, 1024, 64, 1.0)])
+                                         (1, 1, 1024, 64, 1.0), (1, 2, 1280, 64, 1.0), (1, 1, 512, 128, 1.0),
+                                         (12, 16, 100, 64, 1.0), (20, 16, 257, 72, 1 / math.sqrt(72))])
 def test_salience_matches_oracle(lib, B, H, N, d, std):
     from visual_token_sparsity_gb300 import binding as sv
     seed = B * 7 + N

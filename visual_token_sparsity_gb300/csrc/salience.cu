@@ -8,21 +8,34 @@
 //   s[b][j] = 1/(H N) sum_h sum_i exp(scale q_i.k_j - lse_i),
 //   lse_i   = log sum_j exp(scale q_i.k_j).
 //
-// Design (one CTA per (frame, head), 16 softmax warps + 1 TMA/MMA warp):
+// Design: persistent CTAs (one per SM), each walking over (frame, head)
+// units; 16 softmax warps, one MMA-issue warp and one TMA warp.  Per unit two
+// passes run back to back over 128-row tiles x 128-column chunks:
 //   pass 1  K_h resident in shared memory, 128-row tiles of Q_h streamed by
-//           TMA; S = Q_tile K^T (M=128, N<=256 per MMA, K=d padded to 16) goes
-//           to a double-buffered TMEM accumulator; every softmax thread owns
-//           one query row (one TMEM lane) and a quarter of the columns, keeps
-//           an online max / sum of exp2, and the four parts are merged into
-//           lse_i (log2 domain) in shared memory.
-//   The element-wise work is exp-bound: it uses packed fp32x2 FMA/ADD, a
-//   3-input max tree, independent accumulators, and sends a fixed fraction
-//   of the exponentials to an FMA-pipe polynomial (fastmath.cuh) so that
-//   MUFU and the FMA pipe share the load.
+//           TMA; S = Q_tile K_chunk^T (M=128, N<=128, K=d padded to 16) goes
+//           to one of four 128-column TMEM buffers; every softmax thread owns
+//           one query row (one TMEM lane) of the chunk and keeps an online
+//           max / sum of exp2 (log2 domain); per tile the four partial
+//           log-sum-exps of a row are merged into lse_i in shared memory.
 //   pass 2  Q_h resident, 128-row tiles of K_h streamed; S^T = K_tile Q^T puts
 //           one key per TMEM lane, so the column sum over queries becomes a
 //           per-thread row sum of exp2(z - lse_i) with lse_i broadcast from
 //           shared memory.  Padded queries carry lse = +inf and contribute 0.
+// Chunk u of the whole sequence goes to TMEM buffer u % 4 and is consumed by
+// the four warps (one per TMEM lane quarter) of part u % 4, so the four warps
+// that share an SM sub-partition work on different chunks at different times
+// and keep the exp unit busy through each other's TMEM-load latency.
+// The resident operand is replaced chunk by chunk: as soon as the last tile's
+// MMAs on a 128-row chunk complete, the TMA warp loads the next pass's (or the
+// next unit's) rows there, so the tensor pipe never drains between passes.
+// The MMA warp runs its schedule with the whole warp (uniform control flow)
+// and issues from one elected lane; waiting warps sleep inside try_wait.
+// The element-wise work is bound by exp throughput and instruction issue: it
+// uses packed fp32x2 FMA/ADD, a 3-input max tree, a stale running max
+// (rescaled only when it grows by more than 8), one 32-column group in
+// registers at a time and one accumulator chain; variants with
+// double-buffered TMEM loads, more accumulator chains, scalar arithmetic or
+// 256-column buffers measured slower on the SigLIP shape.
 // Shared-memory operands use the K-major no-swizzle layout (8x16-byte core
 // matrices); TMA writes them directly with 8-element x 128-row boxes, and out
 // of range rows are zero-filled by TMA.  Head dims that are not a multiple of
@@ -38,21 +51,26 @@ namespace sv {
 
 namespace {
 
-#ifndef SV_SAL_SOFT_WARPS
-#define SV_SAL_SOFT_WARPS 16
-#endif
-constexpr int kSoftWarps = SV_SAL_SOFT_WARPS;
-constexpr int kParts = kSoftWarps / 4;   // column parts per TMEM lane quarter
-constexpr int kPartCols = 256 / kParts;  // columns of a 256-column chunk per warp
-#ifndef SV_SAL_POLY_PAIRS
-#define SV_SAL_POLY_PAIRS 0
-#endif
-// of every 16 element pairs, this many take exp2 on the FMA pipe, the rest on MUFU
-constexpr int kPolyPairs = SV_SAL_POLY_PAIRS;
-constexpr int kThreads = (kSoftWarps + 1) * 32;
+// Work split (chosen by measurement on the SigLIP shape; see the notes at the
+// top): four 128-column TMEM buffers, each chunk consumed by one softmax warp
+// per lane quarter, 32-column groups loaded one at a time and summed into one
+// fp32x2 accumulator.  The code also handles wider buffers (kBufCols = 256
+// with several warps per buffer quarter), which measured slower.
+constexpr int kBufs = 4;                       // TMEM buffers (one chunk each)
+constexpr int kBufCols = 128;                  // columns of one TMEM buffer (N of one MMA)
+constexpr int kPieces = kBufCols / 128;        // 128-row resident pieces per chunk
+constexpr int kHalves = 1;                     // softmax warps sharing a buffer's lane quarter
+constexpr int kWarpCols = (kBufCols / kHalves + 31) / 32 * 32;  // chunk columns per softmax warp (last may get fewer)
+constexpr int kParts = kBufs * kHalves;        // softmax warps per TMEM lane quarter
+constexpr int kSoftWarps = 4 * kParts;
+constexpr int kSlots = 2;        // streamed 128-row operand tiles in flight
+constexpr int kMmaWarp = kSoftWarps, kTmaWarp = kSoftWarps + 1;
+constexpr int kThreads = (kSoftWarps + 2) * 32;
 constexpr int kTileRows = 128;
-constexpr int kChunkCols = 256;
-constexpr int kTmemCols = 512;
+constexpr int kTmemCols = 512;  // allocations are powers of two; kBufs * kBufCols <= 512
+static_assert(kBufs * kBufCols <= kTmemCols, "TMEM buffers exceed the allocation");
+static_assert(kThreads <= 1024, "block too large");
+constexpr int kMaxChunks = 64;   // resident chunks (N <= 8192; shared memory caps N far lower)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kStatusSalTimeout = 0x10;
 
@@ -61,8 +79,7 @@ struct SalGeom {
   int kc_load;  // 8-element K chunks that TMA loads (d / 8)
   int Np;       // N rounded up to 32 (columns that MMAs produce)
   int Rr;       // N rounded up to 128 (rows of a resident operand)
-  int nt;       // 128-row tiles
-  int nchunks;  // 256-column chunks
+  int nt;       // 128-row tiles = 128-column chunks
   size_t res_bytes, slot_bytes, smem_bytes;
 };
 
@@ -73,10 +90,10 @@ SalGeom sal_geom(int N, int d) {
   g.Np = (N + 31) / 32 * 32;
   g.Rr = (N + kTileRows - 1) / kTileRows * kTileRows;
   g.nt = g.Rr / kTileRows;
-  g.nchunks = (g.Np + kChunkCols - 1) / kChunkCols;
   g.res_bytes = (size_t)g.Rr * g.Kp * 2;
   g.slot_bytes = (size_t)kTileRows * g.Kp * 2;
-  g.smem_bytes = 1024 + g.res_bytes + 2 * g.slot_bytes + (size_t)g.Rr * 4 + 2 * kParts * 256 * 4;
+  // operands, per-part row partials, per-row lse
+  g.smem_bytes = 1024 + g.res_bytes + kSlots * g.slot_bytes + (size_t)kParts * g.Rr * 4 + (size_t)g.Rr * 4;
   return g;
 }
 
@@ -88,34 +105,45 @@ size_t launch_smem(const SalGeom& g) {
 }
 
 struct SalArgs {
-  int N, Kp, kc_load, ks_steps, Np, Rr, nt, nchunks;
+  int N, Kp, kc_load, ks_steps, Np, Rr, nt, units;
   float sl2;  // scale * log2(e)
   float* colsum;
   int* status;
 };
 
 struct SalShared {
-  uint64_t bar_res, bar_pass, bar_done;
-  uint64_t bar_slot[2], bar_free[2], bar_full[2], bar_empty[2];
+  uint64_t bar_done;
+  uint64_t bar_slot[kSlots], bar_slot_free[kSlots];
+  uint64_t bar_full[kBufs], bar_empty[kBufs];
+  uint64_t bar_res[kMaxChunks], bar_res_free[kMaxChunks];
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// Bounded wait: returns immediately once the CTA has aborted.  The timer is
-// read only when the phase is not already complete (reading it is slow).
+constexpr uint32_t kSuspendHintNs = 100000;  // try_wait sleep limit per poll
+// Bounded wait: returns immediately once the CTA has aborted.  A waiting warp
+// sleeps inside try_wait (woken when the phase completes) instead of spinning
+// on issue slots that working warps of the same SM sub-partition need.
 __device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, SalShared& sh) {
   if (ptx::mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = ptx::global_timer();
-  for (uint32_t it = 0;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return;
-    if ((it & 127) == 127) {
-      if (*(volatile int*)&sh.abort_flag) return;
-      if (ptx::global_timer() - t0 > kWaitLimitNs) {
-        *(volatile int*)&sh.abort_flag = 1;
-        return;
-      }
+  for (;;) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return;
+    if (*(volatile int*)&sh.abort_flag) return;
+    if (ptx::global_timer() - t0 > kWaitLimitNs) {
+      *(volatile int*)&sh.abort_flag = 1;
+      return;
     }
   }
+}
+
+// One 128 x nc chunk: KS K-steps of 16, descriptors stepped in their low halves.
+template <int KS>
+__device__ __forceinline__ void mma_chunk(uint32_t d_t, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                          uint32_t a_ks, uint32_t b_ks, uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+    ptx::mma_bf16_split(d_t, a_lo + ks * a_ks, b_lo + ks * b_ks, hi, idesc, ks > 0 ? 1u : 0u);
 }
 
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory"); }
@@ -127,35 +155,39 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
   __shared__ SalShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const int Kp = a.Kp, Rr = a.Rr;
+  const int Kp = a.Kp, Rr = a.Rr, nt = a.nt;
   uint8_t* res = smem;
-  uint8_t* slot[2] = {smem + (size_t)Rr * Kp * 2, smem + (size_t)Rr * Kp * 2 + kTileRows * Kp * 2};
-  float* nlse2 = reinterpret_cast<float*>(slot[1] + kTileRows * Kp * 2);
-  float* mrg = nlse2 + Rr;
+  uint8_t* slots = smem + (size_t)Rr * Kp * 2;
+  const size_t slot_bytes = (size_t)kTileRows * Kp * 2;
+  float* part_lse = reinterpret_cast<float*>(slots + kSlots * slot_bytes);  // [kParts][Rr]
+  float* nlse2 = part_lse + kParts * Rr;                                     // [Rr]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x;
 
   // zero the K chunks that TMA never writes (head dim padded to 16)
   for (int kc = a.kc_load; kc < Kp / 8; ++kc) {
     uint4* r = reinterpret_cast<uint4*>(res + (size_t)kc * Rr * 16);
     for (int i = threadIdx.x; i < Rr; i += blockDim.x) r[i] = make_uint4(0, 0, 0, 0);
-    for (int s = 0; s < 2; ++s) {
-      uint4* p = reinterpret_cast<uint4*>(slot[s] + (size_t)kc * kTileRows * 16);
+    for (int s = 0; s < kSlots; ++s) {
+      uint4* p = reinterpret_cast<uint4*>(slots + s * slot_bytes + (size_t)kc * kTileRows * 16);
       for (int i = threadIdx.x; i < kTileRows; i += blockDim.x) p[i] = make_uint4(0, 0, 0, 0);
     }
   }
   ptx::fence_proxy_async_smem();
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&sh.bar_res, 1);
-    ptx::mbar_init(&sh.bar_pass, 1);
     ptx::mbar_init(&sh.bar_done, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
       ptx::mbar_init(&sh.bar_slot[i], 1);
-      ptx::mbar_init(&sh.bar_free[i], 1);
+      ptx::mbar_init(&sh.bar_slot_free[i], 1);
+    }
+    for (int i = 0; i < kBufs; ++i) {
       ptx::mbar_init(&sh.bar_full[i], 1);
-      ptx::mbar_init(&sh.bar_empty[i], kSoftWarps);
+      ptx::mbar_init(&sh.bar_empty[i], 4 * kHalves);  // the buffer's softmax warps
+    }
+    for (int i = 0; i < nt; ++i) {
+      ptx::mbar_init(&sh.bar_res[i], 1);
+      ptx::mbar_init(&sh.bar_res_free[i], 1);
     }
     sh.abort_flag = 0;
     ptx::mbar_fence_init();
@@ -165,114 +197,136 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
   ptx::tc_fence_after();
   const uint32_t tbase = sh.tmem_base;
 
-  if (warp == kSoftWarps) {
-    // ------------------------------------------------ TMA + MMA issue (one thread)
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------ TMA loads (one thread)
     if (lane == 0) {
       ptx::prefetch_tensormap(&tq);
       ptx::prefetch_tensormap(&tk);
       const uint32_t tile_tx = (uint32_t)a.kc_load * kTileRows * 16;
-      auto load_rows = [&](const CUtensorMap* map, uint8_t* dst, int dst_rows, int row0, int nrows,
+      auto load_rows = [&](const CUtensorMap* map, uint8_t* dst, int dst_rows, int row0, int unit,
                            uint64_t* bar) {
-        ptx::mbar_arrive_expect_tx(bar, tile_tx * (uint32_t)(nrows / kTileRows));
-        for (int r = 0; r < nrows; r += kTileRows)
-          for (int kc = 0; kc < a.kc_load; ++kc)
-            ptx::tma_load_3d(dst + (size_t)kc * dst_rows * 16 + (size_t)r * 16, map, kc * 8,
-                             row0 + r, unit, bar);
+        ptx::mbar_arrive_expect_tx(bar, tile_tx);
+        for (int kc = 0; kc < a.kc_load; ++kc)
+          ptx::tma_load_3d(dst + (size_t)kc * dst_rows * 16, map, kc * 8, row0, unit, bar);
       };
-      uint32_t u = 0;                      // TMEM buffer uses
-      uint32_t slot_waits[2] = {0, 0}, free_waits[2] = {0, 0};
-      const uint32_t res_base = ptx::smem_addr(res);
-      for (int pass = 0; pass < 2; ++pass) {
-        const CUtensorMap* res_map = pass == 0 ? &tk : &tq;
-        const CUtensorMap* str_map = pass == 0 ? &tq : &tk;
-        if (pass == 1) {  // resident operand and slots are rewritten: drain pass-1 MMAs
-          ptx::mma_commit(&sh.bar_pass);
-          wait_bar(&sh.bar_pass, 0, sh);
-        }
-        load_rows(res_map, res, Rr, 0, Rr, &sh.bar_res);
-        load_rows(str_map, slot[0], kTileRows, 0, kTileRows, &sh.bar_slot[0]);
-        if (a.nt > 1) load_rows(str_map, slot[1], kTileRows, kTileRows, kTileRows, &sh.bar_slot[1]);
-        wait_bar(&sh.bar_res, (uint32_t)pass, sh);
-        for (int t = 0; t < a.nt; ++t) {
-          const int s = t & 1;
-          wait_bar(&sh.bar_slot[s], slot_waits[s]++ & 1, sh);
-          const uint32_t a_base = ptx::smem_addr(slot[s]);
-          for (int c = 0; c < a.nchunks; ++c, ++u) {
-            const uint32_t buf = u & 1;
-            if (u >= 2) wait_bar(&sh.bar_empty[buf], ((u >> 1) - 1) & 1, sh);
-            ptx::tc_fence_after();
-            const int nc = min(kChunkCols, a.Np - kChunkCols * c);
-            const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, nc);
-            for (int ks = 0; ks < a.ks_steps; ++ks) {
-              const uint64_t ad = ptx::smem_desc_kmajor(a_base + 2 * ks * kTileRows * 16,
-                                                        kTileRows * 16, 128);
-              const uint64_t bd = ptx::smem_desc_kmajor(
-                  res_base + 2 * ks * Rr * 16 + kChunkCols * c * 16, (uint32_t)Rr * 16, 128);
-              ptx::mma_bf16(tbase + buf * kChunkCols, ad, bd, idesc, ks > 0 ? 1u : 0u);
-            }
-            ptx::mma_commit(&sh.bar_full[buf]);
+      uint32_t g = 0, phase = 0;  // streamed tiles, passes issued so far
+      for (int unit = blockIdx.x; unit < a.units; unit += gridDim.x) {
+        for (int pass = 0; pass < 2; ++pass, ++phase) {
+          const CUtensorMap* res_map = pass == 0 ? &tk : &tq;
+          const CUtensorMap* str_map = pass == 0 ? &tq : &tk;
+          auto load_tile = [&](int t) {
+            const uint32_t gg = g + (uint32_t)t, s = gg % kSlots;
+            if (gg >= kSlots) wait_bar(&sh.bar_slot_free[s], ((gg / kSlots) - 1) & 1, sh);
+            load_rows(str_map, slots + s * slot_bytes, kTileRows, t * kTileRows, unit, &sh.bar_slot[s]);
+          };
+          // the first tile's slot frees before the resident chunks do
+          const int pre = min(kSlots - 1, nt);
+          for (int t = 0; t < pre; ++t) load_tile(t);
+          for (int c = 0; c < nt; ++c) {
+            if (phase > 0) wait_bar(&sh.bar_res_free[c], (phase - 1) & 1, sh);
+            load_rows(res_map, res + (size_t)c * kTileRows * 16, Rr, c * kTileRows, unit, &sh.bar_res[c]);
           }
-          if (t + 2 < a.nt) {
-            ptx::mma_commit(&sh.bar_free[s]);
-            wait_bar(&sh.bar_free[s], free_waits[s]++ & 1, sh);
-            load_rows(str_map, slot[s], kTileRows, (t + 2) * kTileRows, kTileRows,
-                      &sh.bar_slot[s]);
-          }
+          for (int t = pre; t < nt; ++t) load_tile(t);
+          g += (uint32_t)nt;
         }
       }
-      ptx::mma_commit(&sh.bar_done);
-      wait_bar(&sh.bar_done, 0, sh);
     }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------ MMA issue
+    // The whole warp walks the schedule (uniform control flow, so the
+    // descriptors stay warp-uniform); one elected lane issues MMAs and commits.
+    // descriptors: K-major core matrices, 8-row groups 128 B apart; the A
+    // tile's K-adjacent core matrices are 128 rows apart, the resident B's Rr
+    const uint32_t hi = ptx::smem_desc_hi(128);
+    const uint32_t a_lo0 = ptx::smem_desc_lo(ptx::smem_addr(slots), kTileRows * 16);
+    const uint32_t b_lo0 = ptx::smem_desc_lo(ptx::smem_addr(res), (uint32_t)Rr * 16);
+    const uint32_t a_ks = (2 * kTileRows * 16) >> 4, b_ks = (2u * Rr * 16) >> 4;  // one K-step of 16
+    const uint32_t slot_step = (uint32_t)(slot_bytes >> 4), chunk_step = (kBufCols * 16) >> 4;
+    const uint32_t idesc_full = ptx::idesc_bf16_f32(kTileRows, kBufCols);
+    const int nch = (a.Np + kBufCols - 1) / kBufCols;  // chunks of kBufCols keys (queries) per tile
+    const uint32_t idesc_last = ptx::idesc_bf16_f32(kTileRows, a.Np - kBufCols * (nch - 1));
+    const int ks_steps = a.ks_steps;
+    uint32_t u = 0, g = 0, phase = 0;  // chunks, streamed tiles, passes
+    for (int unit = blockIdx.x; unit < a.units; unit += gridDim.x) {
+      for (int pass = 0; pass < 2; ++pass, ++phase) {
+        for (int t = 0; t < nt; ++t, ++g) {
+          const uint32_t s = g % kSlots;
+          wait_bar(&sh.bar_slot[s], (g / kSlots) & 1, sh);
+          const uint32_t a_lo = a_lo0 + s * slot_step;
+          for (int c = 0; c < nch; ++c, ++u) {
+            const uint32_t b = u % kBufs;
+            const int p0 = c * kPieces, p1 = min(nt, p0 + kPieces);  // resident pieces of this chunk
+            if (t == 0)
+              for (int pc = p0; pc < p1; ++pc) wait_bar(&sh.bar_res[pc], phase & 1, sh);
+            if (u >= kBufs) wait_bar(&sh.bar_empty[b], ((u / kBufs) - 1) & 1, sh);
+            ptx::tc_fence_after();
+            const uint32_t idesc = c == nch - 1 ? idesc_last : idesc_full;
+            const uint32_t d_t = tbase + b * kBufCols;
+            const uint32_t b_lo = b_lo0 + (uint32_t)c * chunk_step;
+            if (ptx::elect_one()) {
+              if (ks_steps == 4) mma_chunk<4>(d_t, a_lo, b_lo, hi, a_ks, b_ks, idesc);
+              else if (ks_steps == 5) mma_chunk<5>(d_t, a_lo, b_lo, hi, a_ks, b_ks, idesc);
+              else mma_chunk<8>(d_t, a_lo, b_lo, hi, a_ks, b_ks, idesc);
+              ptx::mma_commit(&sh.bar_full[b]);
+              if (t == nt - 1)
+                for (int pc = p0; pc < p1; ++pc) ptx::mma_commit(&sh.bar_res_free[pc]);
+            }
+            __syncwarp();
+          }
+          if (ptx::elect_one()) ptx::mma_commit(&sh.bar_slot_free[s]);
+          __syncwarp();
+        }
+      }
+    }
+    if (ptx::elect_one()) ptx::mma_commit(&sh.bar_done);
+    __syncwarp();
+    wait_bar(&sh.bar_done, 0, sh);
   } else {
     // ------------------------------------------------ softmax warps
     // warp w reads TMEM lane quarter (w & 3) -- the hardware ties a warp to the
-    // lanes 32 * (w % 4) .. + 31 -- and the column part (w >> 2) of a chunk.
-    const int quarter = warp & 3, part = warp >> 2;
+    // lanes 32 * (w % 4) .. + 31 -- and part p = w >> 2 takes the chunks u
+    // with u % 4 == p % 4, columns [(p / 4) * kWarpCols, + kWarpCols) of each.
+    const int quarter = warp & 3, part = warp >> 2, buf = part % kBufs, half = part / kBufs;
     const int row = quarter * 32 + lane;
-    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int col_lo = half * kWarpCols;
+    const int my_cols = max(0, min(kWarpCols, kBufCols - col_lo));
+    const int nch = (a.Np + kBufCols - 1) / kBufCols;
+    const uint32_t taddr = tbase + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kBufCols + col_lo);
     const float sl2 = a.sl2;
     const uint64_t sl2x2 = fm::splat2(sl2);
+    float* my_part = part_lse + part * Rr;
     uint32_t u = 0;
-    uint32_t ra[32], rb[32];
-    // Runs fn(group registers, column offset) on the warp's ng 32-column
-    // groups starting at TMEM address ta, with the next group's TMEM load in
-    // flight while the current one is processed.
+    uint32_t v[32];
+    // Runs fn(column offset) on each of the ng 32-column groups at TMEM
+    // address ta, the group's values in v.  One group at a time: a single
+    // compact loop body measured faster than double-buffered loads.
     auto for_groups = [&](uint32_t ta, int ng, auto&& fn) {
-      if (ng <= 0) return;
-      ptx::tmem_ld32(ta, ra);
-      ptx::tmem_wait_ld(ra);
-      if (ng > 1) ptx::tmem_ld32(ta + 32, rb);
-      fn(ra, 0);
-      if (ng > 1) {
-        ptx::tmem_wait_ld(rb);
-        if (ng > 2) ptx::tmem_ld32(ta + 64, ra);
-        fn(rb, 32);
-      }
-      if (ng > 2) {
-        ptx::tmem_wait_ld(ra);
-        if (ng > 3) ptx::tmem_ld32(ta + 96, rb);
-        fn(ra, 64);
-      }
-      if (ng > 3) {
-        ptx::tmem_wait_ld(rb);
-        fn(rb, 96);
+      for (int gi = 0; gi < ng; ++gi) {
+        ptx::tmem_ld32(ta + 32 * gi, v);
+        ptx::tmem_wait_ld(v);
+        fn(32 * gi);
       }
     };
-    // pass 1: row log-sum-exp (log2 domain)
-    for (int t = 0; t < a.nt; ++t) {
-      const bool live = t * kTileRows + quarter * 32 < a.N;
-      float m = -INFINITY, l = 0.f;
-      for (int c = 0; c < a.nchunks; ++c, ++u) {
-        const uint32_t buf = u & 1;
-        wait_bar(&sh.bar_full[buf], (u >> 1) & 1, sh);
-        ptx::tc_fence_after();
-        const int nc = min(kChunkCols, a.Np - kChunkCols * c);
-        const int col0 = part * kPartCols;
-        const int ncols = live ? max(0, min(kPartCols, nc - col0)) : 0;
-        {
-          const uint32_t ta = tbase + lane_addr + buf * kChunkCols + col0;
-          for_groups(ta, ncols >> 5, [&](uint32_t* v, int g) {
-            const int key0 = kChunkCols * c + col0 + g;
+    auto chunk_begin = [&]() {
+      wait_bar(&sh.bar_full[buf], (u / kBufs) & 1, sh);
+      ptx::tc_fence_after();
+    };
+    auto chunk_end = [&]() {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
+    };
+    for (int unit = blockIdx.x; unit < a.units; unit += gridDim.x) {
+      // pass 1: per-part row log-sum-exp (log2 domain)
+      for (int t = 0; t < nt; ++t) {
+        const bool live = t * kTileRows + quarter * 32 < a.N;
+        float m = -INFINITY, l = 0.f;
+        for (int c = 0; c < nch; ++c, ++u) {
+          if ((int)(u % kBufs) != buf) continue;
+          chunk_begin();
+          const int nc = min(my_cols, a.Np - kBufCols * c - col_lo);
+          for_groups(taddr, live && nc > 0 ? nc >> 5 : 0, [&](int g) {
+            const int key0 = kBufCols * c + col_lo + g;
             if (key0 + 32 > a.N) {
 #pragma unroll
               for (int i = 0; i < 32; ++i)
@@ -296,86 +350,69 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             }
             if (m == -INFINITY) return;
             const uint64_t nmn = fm::splat2(-m);
-            uint64_t acc[4] = {0, 0, 0, 0};
+            uint64_t acc = 0;
 #pragma unroll
             for (int pr = 0; pr < 16; ++pr) {
               const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
                                           sl2x2, nmn);
-              const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
-              acc[pr & 3] = fm::add2(acc[pr & 3], e);
+              acc = fm::add2(acc, fm::exp2_mufu2(x));
             }
-            const uint64_t s2 = fm::add2(fm::add2(acc[0], acc[1]), fm::add2(acc[2], acc[3]));
             float s0, s1;
-            fm::unpack2(s2, s0, s1);
+            fm::unpack2(acc, s0, s1);
             l += s0 + s1;
           });
+          chunk_end();
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
+        my_part[t * kTileRows + row] = m == -INFINITY ? -INFINITY : m + __log2f(l);
       }
-      float* mg = mrg + (t & 1) * (kParts * 256);
-      mg[part * 256 + row * 2] = m;
-      mg[part * 256 + row * 2 + 1] = l;
       softmax_bar();
-      if (part == 0) {
+      for (int r = threadIdx.x; r < Rr; r += kSoftWarps * 32) {
         float M = -INFINITY;
 #pragma unroll
-        for (int p2 = 0; p2 < kParts; ++p2) M = fmaxf(M, mg[p2 * 256 + row * 2]);
+        for (int p = 0; p < kParts; ++p) M = fmaxf(M, part_lse[p * Rr + r]);
         float L = 0.f;
 #pragma unroll
-        for (int p2 = 0; p2 < kParts; ++p2) {
-          const float mp = mg[p2 * 256 + row * 2];
-          if (mp != -INFINITY) L += mg[p2 * 256 + row * 2 + 1] * fm::ex2_mufu(mp - M);
+        for (int p = 0; p < kParts; ++p) {
+          const float lp = part_lse[p * Rr + r];
+          if (lp != -INFINITY) L += fm::ex2_mufu(lp - M);
         }
-        const int qi = t * kTileRows + row;
         // stored negated: pass 2 adds it with one packed FMA; padded queries
         // get -inf and contribute nothing
-        nlse2[qi] = qi < a.N ? -(M + __log2f(L)) : -INFINITY;
+        nlse2[r] = r < a.N ? -(M + __log2f(L)) : -INFINITY;
       }
-    }
-    softmax_bar();
-    // pass 2: column sums of exp2(z - lse), one key per TMEM lane
-    for (int t = 0; t < a.nt; ++t) {
-      const bool live = t * kTileRows + quarter * 32 < a.N;
-      uint64_t acc[4] = {0, 0, 0, 0};
-      for (int c = 0; c < a.nchunks; ++c, ++u) {
-        const uint32_t buf = u & 1;
-        wait_bar(&sh.bar_full[buf], (u >> 1) & 1, sh);
-        ptx::tc_fence_after();
-        const int nc = min(kChunkCols, a.Np - kChunkCols * c);
-        const int col0 = part * kPartCols;
-        const int ncols = live ? max(0, min(kPartCols, nc - col0)) : 0;
-        {
-          const uint32_t ta = tbase + lane_addr + buf * kChunkCols + col0;
-          for_groups(ta, ncols >> 5, [&](const uint32_t* v, int g) {
-            const uint64_t* nl = reinterpret_cast<const uint64_t*>(nlse2 + kChunkCols * c + col0 + g);
+      softmax_bar();
+      // pass 2: column sums of exp2(z - lse), one key per TMEM lane
+      for (int t = 0; t < nt; ++t) {
+        const bool live = t * kTileRows + quarter * 32 < a.N;
+        uint64_t acc = 0;
+        for (int c = 0; c < nch; ++c, ++u) {
+          if ((int)(u % kBufs) != buf) continue;
+          chunk_begin();
+          const int nc = min(my_cols, a.Np - kBufCols * c - col_lo);
+          for_groups(taddr, live && nc > 0 ? nc >> 5 : 0, [&](int g) {
+            // lse of the group's 32 queries: the same for every lane (broadcast)
+            const uint64_t* nl = reinterpret_cast<const uint64_t*>(nlse2 + kBufCols * c + col_lo + g);
 #pragma unroll
             for (int pr = 0; pr < 16; ++pr) {
               const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
                                           sl2x2, nl[pr]);
-              const uint64_t e = pr < kPolyPairs ? fm::exp2_poly2(x) : fm::exp2_mufu2(x);
-              acc[pr & 3] = fm::add2(acc[pr & 3], e);
+              acc = fm::add2(acc, fm::exp2_mufu2(x));
             }
           });
+          chunk_end();
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
+        float s0, s1;
+        fm::unpack2(acc, s0, s1);
+        my_part[t * kTileRows + row] = s0 + s1;
       }
-      const uint64_t s2 = fm::add2(fm::add2(acc[0], acc[1]), fm::add2(acc[2], acc[3]));
-      float s0, s1;
-      fm::unpack2(s2, s0, s1);
-      float* mg = mrg + (t & 1) * (kParts * 128);
-      mg[part * 128 + row] = s0 + s1;
       softmax_bar();
-      if (part == 0) {
-        const int key = t * kTileRows + row;
+      for (int r = threadIdx.x; r < a.N; r += kSoftWarps * 32) {
         float tot = 0.f;
 #pragma unroll
-        for (int p2 = 0; p2 < kParts; ++p2) tot += mg[p2 * 128 + row];
-        if (key < a.N) a.colsum[(size_t)unit * a.N + key] = tot;
+        for (int p = 0; p < kParts; ++p) tot += part_lse[p * Rr + r];
+        a.colsum[(size_t)unit * a.N + r] = tot;
       }
+      softmax_bar();  // the partials are rewritten by the next unit's pass 1
     }
   }
   __syncthreads();
@@ -440,8 +477,8 @@ size_t salience_workspace_bytes(int B, int H, int N, int d) {
 cudaError_t launch_salience(const void* q, const void* k, int B, int H, int N, int d, float scale,
                             float* salience, void* ws, int* status, int num_sms,
                             cudaStream_t stream) {
-  (void)num_sms;
   const SalGeom g = sal_geom(N, d);
+  if (g.nt > kMaxChunks) return cudaErrorInvalidValue;
   CUtensorMap tq, tk;
   if (!make_map(&tq, q, d, N, B * H) || !make_map(&tk, k, d, N, B * H)) return cudaErrorInvalidValue;
   SalArgs a;
@@ -452,7 +489,7 @@ cudaError_t launch_salience(const void* q, const void* k, int B, int H, int N, i
   a.Np = g.Np;
   a.Rr = g.Rr;
   a.nt = g.nt;
-  a.nchunks = g.nchunks;
+  a.units = B * H;
   a.sl2 = scale * kLog2e;
   a.colsum = static_cast<float*>(ws);
   a.status = status;
@@ -460,7 +497,8 @@ cudaError_t launch_salience(const void* q, const void* k, int B, int H, int N, i
   cudaError_t e = cudaFuncSetAttribute(salience_colsum_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  salience_colsum_kernel<<<B * H, kThreads, smem, stream>>>(tq, tk, a);
+  const int grid = a.units < num_sms ? a.units : num_sms;
+  salience_colsum_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long total = (long long)B * N;
