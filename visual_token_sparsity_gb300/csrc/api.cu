@@ -170,7 +170,7 @@ sv_status sv_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx
   if (s != SV_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // long rows: a cluster of CTAs per row; otherwise one CTA per row
-  const cudaError_t e = (n > 16384 && sv::topk_cluster_fits(n))
+  const cudaError_t e = sv::topk_prefers_cluster(n)
                             ? sv::launch_topk_cluster(scores, rows, n, k, idx, st)
                             : sv::launch_topk_rows(scores, rows, n, k, idx, st);
   return cuda_status(e, "sv_topk_rows");

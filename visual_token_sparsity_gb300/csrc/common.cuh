@@ -9,6 +9,7 @@ namespace sv {
 constexpr int kBlockTokens = 16;
 constexpr int kStatusBadBlock = 0x1;
 constexpr int kStatusBadIndex = 0x2;
+constexpr int kStatusTimeout = 0x10;   // a bounded wait inside a kernel gave up
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void flag_status(int* status, int bits) { atomicOr(status, bits); }

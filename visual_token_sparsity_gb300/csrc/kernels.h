@@ -20,6 +20,7 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
 cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
                              cudaStream_t stream);
 bool topk_cluster_fits(int n);
+bool topk_prefers_cluster(int n);   // long rows that fit: use launch_topk_cluster
 cudaError_t launch_topk_cluster(const float* scores, int rows, int n, int k, int32_t* idx,
                                 cudaStream_t stream);
 

@@ -170,7 +170,7 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
         vis_idx);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || fuse) return e;
-  if (topk_cluster_fits(n_vis)) return launch_topk_cluster(scores, rows, n_vis, k, vis_idx, stream);
+  if (topk_prefers_cluster(n_vis)) return launch_topk_cluster(scores, rows, n_vis, k, vis_idx, stream);
   return launch_topk_rows(scores, rows, n_vis, k, vis_idx, stream);
 }
 

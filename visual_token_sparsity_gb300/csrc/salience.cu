@@ -72,7 +72,6 @@ static_assert(kBufs * kBufCols <= kTmemCols, "TMEM buffers exceed the allocation
 static_assert(kThreads <= 1024, "block too large");
 constexpr int kMaxChunks = 64;   // resident chunks (N <= 8192; shared memory caps N far lower)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kStatusSalTimeout = 0x10;
 
 struct SalGeom {
   int Kp;       // padded head dim (multiple of 16)
@@ -416,7 +415,7 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && sh.abort_flag) flag_status(a.status, kStatusSalTimeout);
+  if (threadIdx.x == 0 && sh.abort_flag) flag_status(a.status, kStatusTimeout);
   if (warp == 0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tbase, kTmemCols);

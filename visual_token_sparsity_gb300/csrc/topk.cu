@@ -29,7 +29,7 @@ cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_
   if (rows == 0) return cudaSuccess;
   const bool in_smem = n <= topk_max_smem_keys();
   const size_t smem = in_smem ? (size_t)n * sizeof(uint32_t) : 0;
-  const int threads = n >= 16384 ? 1024 : (n >= 2048 ? 512 : 256);
+  const int threads = n >= 16384 ? 1024 : (n >= 8192 ? 512 : 256);
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
