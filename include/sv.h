@@ -57,6 +57,7 @@ typedef enum {
 /* Device status bits (the status word is the first int32 of a workspace). */
 #define SV_DEV_BAD_BLOCK 0x1   /* a block-table entry outside [0, num_blocks) */
 #define SV_DEV_BAD_INDEX 0x2   /* a visual index outside [0, n_vis) */
+#define SV_DEV_TIMEOUT   0x10  /* a bounded wait inside a kernel gave up (2 s); results undefined */
 
 /* Tokens per KV page (fixed). */
 #define SV_BLOCK_TOKENS 16
