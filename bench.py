@@ -141,8 +141,10 @@ def measured_traffic(call):
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path))[call]
-        src = os.path.join(ROOT, rec["source"])
-        if hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
+        h = hashlib.sha1()
+        for src in rec["sources"]:      # every file the kernel is built from
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        if h.hexdigest() != rec["sources_sha1"]:
             return None
         return rec["bytes_per_launch"]
     except Exception:
