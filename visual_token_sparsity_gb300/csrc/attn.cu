@@ -69,15 +69,21 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   long long min_tpw = (tiles + kAttnMaxSplits - 1) / kAttnMaxSplits;
   if (tpw < min_tpw) tpw = min_tpw;
   // small tiles (large G): at least 128 tokens per split, or the partials
-  // (G x (d + 2) floats per split) and their merge dominate
-  const long long min_tokens = attn_uses_mma(G) ? 128 : 0;
+  // (G x (d + 2) floats per split) and their merge dominate; with 16 or more
+  // (sequence, KV head) units there is parallelism enough for 256, which
+  // halves each warp's share of fixed costs (row-id resolution, pipeline
+  // fill, partial write)
+  const long long min_tokens = attn_uses_mma(G) ? (units >= 16 ? 256 : 128) : 0;
   if (tpw * p.tile < min_tokens) tpw = (min_tokens + p.tile - 1) / p.tile;
   p.chunk = (int)(tpw * p.tile);
   p.nsplit = n_tokens > 0 ? (n_tokens + p.chunk - 1) / p.chunk : 1;
   // nsplit <= ceil(tiles / tpw) <= min(tiles, ceil(target / units), max): a
   // bound that never decreases as n_tokens grows (workspace sizing).
   // chunk >= max(tile, min_tokens), so nsplit <= ceil(n_tokens / that)
-  const long long min_chunk = min_tokens > p.tile ? (min_tokens + p.tile - 1) / p.tile * p.tile : p.tile;
+  // (the bound takes the smaller split minimum, 128, whatever `units` is)
+  const long long min_bound_tokens = attn_uses_mma(G) ? 128 : 0;
+  const long long min_chunk =
+      min_bound_tokens > p.tile ? (min_bound_tokens + p.tile - 1) / p.tile * p.tile : p.tile;
   long long ub = (n_tokens + min_chunk - 1) / min_chunk;
   if (ub < 1) ub = 1;
   const long long per_unit = (kAttnTargetWarps + units - 1) / (units > 0 ? units : 1);
