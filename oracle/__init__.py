@@ -32,6 +32,7 @@ from .sparsevila import (  # noqa: F401
     retrieval_scores,
     retrieve_topk,
     sparse_decode_attention,
+    pack_selected_kv,
     evict_qa_tokens,
     append_tokens,
 )

@@ -188,6 +188,33 @@ def sparse_decode_attention(q, K, V, vis_idx, n_vis, n_text, scale=None):
     return out, lse
 
 
+def pack_selected_kv(K, V, vis_idx, n_vis, n_text):
+    """Pack-once KV: the retrieved visual tokens and the text, contiguous.
+
+    velog.io summary §3.2 (why decode-time selection is efficient): the
+    selected KV entries are gathered into contiguous memory so the attention
+    reads them with regular, coalesced accesses.  Per (sequence b, KV head g)
+    the packed cache holds the selected visual tokens in vis_idx[b, g] order,
+    then the n_text text tokens in their order.
+
+    K, V: logical [B][Hkv][>= n_vis + n_text][d]; vis_idx: [B][Hkv][k] or None
+    (= every visual token).  Returns logical K', V' [B][Hkv][k + n_text][d].
+    """
+    K = np.asarray(K)
+    V = np.asarray(V)
+    B, Hkv = K.shape[0], K.shape[1]
+    k = n_vis if vis_idx is None else np.asarray(vis_idx).shape[2]
+    Kp = np.empty((B, Hkv, k + n_text, K.shape[3]), dtype=K.dtype)
+    Vp = np.empty_like(Kp)
+    for b in range(B):
+        for g in range(Hkv):
+            vis = np.arange(n_vis) if vis_idx is None else np.asarray(vis_idx[b, g], dtype=np.int64)
+            tokens = np.concatenate([vis, np.arange(n_vis, n_vis + n_text, dtype=np.int64)])
+            Kp[b, g] = K[b, g, tokens]
+            Vp[b, g] = V[b, g, tokens]
+    return Kp, Vp
+
+
 def evict_qa_tokens(K, V, n_vis, n_text, text_begin, text_end):
     """Partial KV-cache eviction between conversation rounds.
 

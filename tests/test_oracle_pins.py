@@ -276,6 +276,46 @@ def _logical(B=1, Hkv=2, n=12, d=2):
     return x.copy(), -x.copy()
 
 
+def test_pack_all_visual_is_the_prefix_of_the_cache():
+    K = RNG.standard_normal((2, 3, 13, 4))
+    V = RNG.standard_normal((2, 3, 13, 4))
+    Kp, Vp = oracle.pack_selected_kv(K, V, None, n_vis=9, n_text=3)
+    np.testing.assert_array_equal(Kp, K[:, :, :12])
+    np.testing.assert_array_equal(Vp, V[:, :, :12])
+
+
+def test_pack_order_and_head_map_by_token_id_encoding():
+    # every row encodes (sequence, head, token, tensor) so the packed rows can
+    # be decoded back to where they came from
+    B, Hkv, n_vis, n_text, d = 2, 3, 10, 4, 3
+    K = np.zeros((B, Hkv, n_vis + n_text + 2, d))
+    for b, g, t in itertools.product(range(B), range(Hkv), range(K.shape[2])):
+        K[b, g, t] = (b, g, t)
+    V = -K
+    vis = np.stack([np.stack([np.sort(RNG.choice(n_vis, 4, replace=False)) for _ in range(Hkv)])
+                    for _ in range(B)])
+    Kp, Vp = oracle.pack_selected_kv(K, V, vis, n_vis, n_text)
+    assert Kp.shape == (B, Hkv, 4 + n_text, d)
+    for b, g in itertools.product(range(B), range(Hkv)):
+        assert (Kp[b, g, :, 0] == b).all() and (Kp[b, g, :, 1] == g).all()
+        assert list(Kp[b, g, :, 2]) == list(vis[b, g]) + list(range(n_vis, n_vis + n_text))
+    np.testing.assert_array_equal(Vp, -Kp)
+
+
+def test_dense_attention_over_packed_equals_sparse_attention():
+    B, H, Hkv, n_vis, n_text, d = 2, 6, 2, 20, 5, 8
+    K = RNG.standard_normal((B, Hkv, n_vis + n_text, d))
+    V = RNG.standard_normal((B, Hkv, n_vis + n_text, d))
+    q = RNG.standard_normal((B, H, d))
+    vis = np.stack([np.stack([np.sort(RNG.choice(n_vis, 7, replace=False)) for _ in range(Hkv)])
+                    for _ in range(B)])
+    ref, ref_lse = oracle.sparse_decode_attention(q, K, V, vis, n_vis, n_text)
+    Kp, Vp = oracle.pack_selected_kv(K, V, vis, n_vis, n_text)
+    got, got_lse = oracle.sparse_decode_attention(q, Kp, Vp, None, 7, n_text)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got_lse, ref_lse, rtol=0, atol=1e-12)
+
+
 def test_evict_tail_span_truncates():
     K, V = _logical(n=12)
     K2, V2, nt = oracle.evict_qa_tokens(K, V, n_vis=5, n_text=7, text_begin=3, text_end=7)
