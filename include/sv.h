@@ -228,6 +228,32 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
                                 void* out, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Pack-once KV for round reuse -- velog.io summary §3.2 (why decode-time
+ * selection is efficient: the selected KV entries are gathered into
+ * contiguous memory so the attention reads them with coalesced accesses).
+ *
+ * For every sequence b and KV head g, copies the K/V rows of the selected
+ * visual tokens vis_idx[b][g][0..k) (in that order; NULL = all n_vis visual
+ * tokens, k ignored) followed by the seqs->n_text text tokens of `src` to
+ * logical positions [0, k + n_text) of sequence b in `dst`, addressed
+ * through dst_seqs->block_table.  Afterwards
+ *   sv_sparse_decode_attn(q, H, scale, dst, dst_seqs, NULL, 0, ...)
+ * attends over the same tokens, in the same order and with the same split
+ * plan, as sv_sparse_decode_attn(q, H, scale, src, seqs, vis_idx, k, ...),
+ * and so returns the same bits, reading whole contiguous pages; later
+ * decode tokens are appended to dst with sv_kv_append(dst, dst_seqs, ...).
+ * src, seqs : the paged cache and its batch view (read only).
+ * dst       : a second paged layer (own pools, same n_kv_heads / head_dim).
+ * dst_seqs  : batch = seqs->batch, n_vis = k, n_text = seqs->n_text; its
+ *             block table must cover k + n_text positions per sequence.
+ * ws        : sv_evict_workspace_bytes() (the status word).
+ * Device-side index / block errors set the status bits and skip the row.
+ */
+sv_status sv_pack_kv(const sv_kv_layer* src, const sv_seq_batch* seqs, const int32_t* vis_idx, int k,
+                     const sv_kv_layer* dst, const sv_seq_batch* dst_seqs, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/*
  * Partial KV-cache eviction between rounds -- velog.io summary §4.1 Setup
  * (after each round only the previous question/answer KV entries are removed;
  * the visual cache stays); xllm-io review §五 partial_kv_cache_eviction.

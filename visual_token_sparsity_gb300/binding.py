@@ -64,6 +64,8 @@ _SIGS = {
                                 ctypes.c_int32, ctypes.c_int32, _VP, _VP, _SZ, _VP]),
     "sv_kv_append": (_I, [ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch), _VP, _VP, _I,
                           _VP, _SZ, _VP]),
+    "sv_pack_kv": (_I, [ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch), _VP, _I,
+                        ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch), _VP, _SZ, _VP]),
     "sv_read_device_status": (_I, [_VP, _I, ctypes.POINTER(ctypes.c_int32), _VP]),
 }
 EXPORTED = tuple(_SIGS)
@@ -257,6 +259,14 @@ def sv_kv_append(layer, seqs, k_new, v_new, ws, stream=None):
     T = k_new.shape[1]
     _check(lib.sv_kv_append(ctypes.byref(layer.c), ctypes.byref(seqs.c), _ptr(k_new, torch.bfloat16, "k_new"),
                             _ptr(v_new, torch.bfloat16, "v_new"), T, *_ws(ws), _stream(stream)))
+
+
+def sv_pack_kv(src, seqs, vis_idx, k, dst, dst_seqs, ws, stream=None):
+    """Copy the selected visual (vis_idx int32 [B][Hkv][k], or None = all) and all
+    text K/V rows of src to positions [0, k + n_text) of dst (see include/sv.h)."""
+    lib = load()
+    _check(lib.sv_pack_kv(ctypes.byref(src.c), ctypes.byref(seqs.c), _ptr(vis_idx, torch.int32, "vis_idx"), int(k),
+                          ctypes.byref(dst.c), ctypes.byref(dst_seqs.c), *_ws(ws), _stream(stream)))
 
 
 def sv_read_device_status(ws, clear=False, stream=None):

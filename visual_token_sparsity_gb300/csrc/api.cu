@@ -260,6 +260,32 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
 
 // ------------------------------------------------------------------ rounds
 
+sv_status sv_pack_kv(const sv_kv_layer* src, const sv_seq_batch* seqs, const int32_t* vis_idx, int k,
+                     const sv_kv_layer* dst, const sv_seq_batch* dst_seqs, void* ws, size_t ws_bytes,
+                     void* stream) {
+  sv_status s = check_cache(src, seqs, true);
+  if (s != SV_OK) return s;
+  s = check_cache(dst, dst_seqs, true);
+  if (s != SV_OK) return s;
+  if (dst->n_kv_heads != src->n_kv_heads || dst->head_dim != src->head_dim)
+    return fail(SV_ERR_INVALID_ARG, "source and packed layers differ in n_kv_heads or head_dim");
+  if (dst->k_pool == src->k_pool || dst->v_pool == src->v_pool)
+    return fail(SV_ERR_INVALID_ARG, "the packed layer must not share pools with the source");
+  const int k_vis = vis_idx ? k : seqs->n_vis;
+  if (vis_idx && (k < 0 || k > seqs->n_vis)) return fail(SV_ERR_INVALID_ARG, "need 0 <= k <= n_vis");
+  if (dst_seqs->batch != seqs->batch || dst_seqs->n_vis != k_vis || dst_seqs->n_text != seqs->n_text)
+    return fail(SV_ERR_INVALID_ARG,
+                "packed batch must have the source's batch, n_vis = k (%d) and n_text = %d", k_vis, seqs->n_text);
+  s = check_ws(ws, ws_bytes, sv_evict_workspace_bytes());
+  if (s != SV_OK) return s;
+  cudaError_t e = sv::launch_pack_kv(src->k_pool, src->v_pool, src->num_blocks, seqs->block_table,
+                                     seqs->max_blocks, seqs->n_vis, vis_idx, k_vis, seqs->n_text, dst->k_pool,
+                                     dst->v_pool, dst->num_blocks, dst_seqs->block_table, dst_seqs->max_blocks,
+                                     seqs->batch, src->n_kv_heads, src->head_dim, status_word(ws),
+                                     static_cast<cudaStream_t>(stream));
+  return cuda_status(e, "sv_pack_kv");
+}
+
 sv_status sv_evict_qa_tokens(const sv_kv_layer* layers, int n_layers, sv_seq_batch* seqs,
                              int32_t text_begin, int32_t text_end, int32_t* n_blocks_in_use,
                              void* ws, size_t ws_bytes, void* stream) {

@@ -24,6 +24,14 @@ bool topk_prefers_cluster(int n);   // long rows that fit: use launch_topk_clust
 cudaError_t launch_topk_cluster(const float* scores, int rows, int n, int k, int32_t* idx,
                                 cudaStream_t stream);
 
+// ---- pack-once KV (pack.cu): selected visual + text rows of src copied to
+// positions [0, k + n_text) of every sequence of dst (same Hkv and D)
+cudaError_t launch_pack_kv(const void* k_src, const void* v_src, int src_blocks, const int32_t* src_bt,
+                           int src_max_blocks, int n_vis, const int32_t* vis_idx, int k, int n_text,
+                           void* k_dst, void* v_dst, int dst_blocks, const int32_t* dst_bt,
+                           int dst_max_blocks, int batch, int Hkv, int D, int* status,
+                           cudaStream_t stream);
+
 // ---- sparse decode attention (attn.cu)
 struct AttnPlan {
   int tile;
