@@ -58,6 +58,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-decode", action="store_true", help="salience measurement only")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-packed", action="store_true", help="skip the pack-once KV comparison")
     return p.parse_args()
 
 
@@ -221,6 +222,31 @@ class DecodeWorkload:
     def attn_only_step(self):
         for l in range(self.shape.layers):
             self.attend(l)
+
+    # pack-once KV: per layer a second paged layer holding, per (sequence, KV
+    # head), the selected visual rows then the text rows contiguously
+    def make_packed(self):
+        sv, s = self.sv, self.shape
+        n = s.k + s.n_text
+        nblk = (n + 15) // 16
+        bt = torch.arange(s.batch * nblk, dtype=torch.int32, device=self.dev).view(s.batch, nblk)
+        self.pseqs = sv.SeqBatch(bt, s.k, s.n_text)
+        self.players = []
+        for l in range(s.layers):
+            kp = torch.empty(s.batch * nblk, s.Hkv, 16, s.d, dtype=torch.bfloat16, device=self.dev)
+            self.players.append(sv.KvLayer(kp, torch.empty_like(kp)))
+        self.ws_p = sv.workspace(256, self.dev)
+
+    def pack_all(self):
+        for l in range(self.shape.layers):
+            self.sv.sv_pack_kv(self.layers[l], self.seqs, self.vis[l], self.shape.k, self.players[l], self.pseqs,
+                               self.ws_p)
+
+    def attn_packed_step(self):
+        s = self.shape
+        for l in range(s.layers):
+            self.sv.sv_sparse_decode_attn(self.q_dec[l], self.scale, self.players[l], self.pseqs, None, 0,
+                                          self.out[l], None, self.ws_a)
 
 
 def time_graph(fn, steps, warmup, stream):
@@ -412,13 +438,41 @@ def rounds_main(a):
             seqs.n_text += 1
             sv.sv_sparse_decode_attn(aq[t], scale, layer, seqs, vis, s.k, outs[t], None, ws_a)
 
+    # pack-once variant: after the retrieval the selected visual rows and the
+    # text are packed into a second paged layer, the answer tokens are appended
+    # there and every decode step attends densely over it
+    n_pack = s.k + 32 + 32 + 256
+    pblk = (n_pack + 15) // 16
+    pbt = torch.arange(B * pblk, dtype=torch.int32, device=dev).view(B, pblk)
+    pk_pool = torch.empty(B * pblk, Hkv, 16, d, dtype=torch.bfloat16, device=dev)
+    player = sv.KvLayer(pk_pool, torch.empty_like(pk_pool))
+    outs_p = torch.empty_like(outs)
+
+    def one_round_packed():
+        seqs = sv.SeqBatch(bt, s.n_vis, 32 + 32 + 256)
+        sv.sv_evict_qa_tokens([layer], seqs, 32, seqs.n_text, ws_e)
+        sv.sv_kv_append(layer, seqs, qk, qv, ws_e)
+        seqs.n_text += 32
+        sv.sv_retrieve_topk(rows, layer, seqs, s.k, vis, None, ws_r)
+        pseqs = sv.SeqBatch(pbt, s.k, seqs.n_text)
+        sv.sv_pack_kv(layer, seqs, vis, s.k, player, pseqs, ws_e)
+        for t in range(256):
+            sv.sv_kv_append(player, pseqs, ak_steps[t], av_steps[t], ws_e)
+            pseqs.n_text += 1
+            sv.sv_sparse_decode_attn(aq[t], scale, player, pseqs, None, 0, outs_p[t], None, ws_a)
+
     stream = torch.cuda.Stream()
     graph = time_graph(one_round, a.steps, max(3, a.warmup), stream)
     ms = replay_timed(graph, a.steps, stream, lambda: None)
+    graph_p = time_graph(one_round_packed, a.steps, max(3, a.warmup), stream)
+    ms_p = replay_timed(graph_p, a.steps, stream, lambda: None)
     print(json.dumps({"metric": "multi-turn round latency (tiny shapes)", "value": ms * 1e3, "unit": "us/round",
                       "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "higher_is_better": False,
                       "per_decode_step_us": ms * 1e3 / 256, "dtype": "bf16", "data": "synthetic",
                       "gpu_launches": a.steps * (1 + 1 + 256 * 2),
+                      "packed": {"round_us": ms_p * 1e3, "per_decode_step_us": ms_p * 1e3 / 256,
+                                 "note": "same round with the selection packed once (sv_pack_kv) and dense "
+                                         "attention over the packed pages"},
                       "config": {"workload": "round loop: evict, append 32-token question, retrieve top-25% "
                                              "with 32 rows, 256 x (append + sparse attention); 4 q / 2 KV "
                                              "heads, d 64, 576 visual + 32-token prefix", "batch": s.batch}}))
@@ -549,6 +603,22 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
     if not a.no_e2e:
         e2e, h2d, d2h = e2e_throughput(wl, min(50, max(3, a.steps // 2)), 2, stream, bytes_step)
         line["e2e"] = {"value": world * e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if not a.no_packed:
+        # pack-once KV (round reuse): the selected rows of every layer are
+        # packed once per round, then each decode step attends densely
+        wl.make_packed()
+        g_pack = time_graph(wl.pack_all, a.steps, 3, stream)
+        g_dense = time_graph(wl.attn_packed_step, a.steps, 3, stream)
+        ms_pack = replay_timed(g_pack, a.steps, stream, barrier)
+        ms_dense = replay_timed(g_dense, a.steps, stream, barrier)
+        line["packed"] = {
+            "attn_only_step_us": ms_dense * 1e3, "gather_attn_only_step_us": ms_attn * 1e3,
+            "attention_gbs": ab / (ms_dense * 1e-3) / 1e9, "gather_attention_gbs": ab / (ms_attn * 1e-3) / 1e9,
+            "pack_all_layers_us": ms_pack * 1e3,
+            "step_us_amortized_256": (ms_dense + ms_pack / 256) * 1e3,
+            "note": "attention over the retrieval's selection; pack once per round (all layers), "
+                    "then dense attention over the packed pages each decode step"}
+        del g_pack, g_dense
     del wl, g_step, g_attn
     torch.cuda.empty_cache()
 
