@@ -26,6 +26,7 @@ invariants, brute force on tiny inputs, library routines); none is
 from .sparsevila import (  # noqa: F401
     BLOCK_TOKENS,
     salience,
+    summary_salience,
     topk_ascending,
     prune_compact,
     paged_view,

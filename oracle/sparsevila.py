@@ -59,6 +59,35 @@ def salience(q, k, scale=None):
     return s / (H * N)
 
 
+def summary_salience(q, k, R, scale=None):
+    """Query-agnostic salience for encoders with summary tokens.
+
+    velog.io summary §3.1 (encoder-type table): with a single summary token
+    (CLIP) a token's importance is the attention it contributes to the global
+    embedding, i.e. the summary token's attention to it; with several
+    summary tokens (RADIO) it is the mean attention toward them.  Reading
+    taken: the R summary tokens are the first R tokens of the sequence; per
+    head, the summary rows of the row-softmax of Z = scale * Q K^T (softmax
+    over all N tokens) are averaged over the R rows and the H heads.
+
+    q, k: [B][H][N][d].  Returns s: [B][N] with s[b].sum() == 1.
+    """
+    q = _as_f64(q)
+    k = _as_f64(k)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    s = np.zeros((B, N), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            z = scale * (q[b, h, :R] @ k[b, h].T)         # [R summary rows][N keys]
+            z = z - z.max(axis=1, keepdims=True)
+            p = np.exp(z)
+            p = p / p.sum(axis=1, keepdims=True)
+            s[b] += p.sum(axis=0)
+    return s / (H * R)
+
+
 def topk_ascending(scores, k):
     """Indices of the k largest entries of every row, in ascending order.
 

@@ -29,6 +29,34 @@ def test_salience_rows_stochastic_sum_to_one():
     assert (s > 0).all()
 
 
+def test_summary_salience_single_row_is_torch_softmax_row():
+    q = RNG.standard_normal((2, 3, 9, 4))
+    k = RNG.standard_normal((2, 3, 9, 4))
+    s = oracle.summary_salience(q, k, 1)
+    zt = torch.einsum("bhd,bhnd->bhn", torch.from_numpy(q[:, :, 0]), torch.from_numpy(k)) / 2.0
+    ref = torch.softmax(zt, dim=-1).mean(dim=1).numpy()          # head mean of the CLS row
+    np.testing.assert_allclose(s, ref, rtol=0, atol=1e-14)
+
+
+def test_summary_salience_all_rows_is_full_salience_and_rows_sum_to_one():
+    q = RNG.standard_normal((1, 2, 7, 3))
+    k = RNG.standard_normal((1, 2, 7, 3))
+    np.testing.assert_allclose(oracle.summary_salience(q, k, 7), oracle.salience(q, k), rtol=0, atol=1e-14)
+    s = oracle.summary_salience(q, k, 3)
+    np.testing.assert_allclose(s.sum(-1), 1.0, rtol=0, atol=1e-13)
+
+
+def test_summary_salience_uses_only_leading_rows_and_zero_query_is_uniform():
+    q = RNG.standard_normal((1, 2, 6, 4))
+    k = RNG.standard_normal((1, 2, 6, 4))
+    q2 = q.copy()
+    q2[:, :, 2:] = RNG.standard_normal((1, 2, 4, 4))                # non-summary rows do not matter
+    np.testing.assert_array_equal(oracle.summary_salience(q, k, 2), oracle.summary_salience(q2, k, 2))
+    q3 = q.copy()
+    q3[:, :, :2] = 0.0
+    np.testing.assert_allclose(oracle.summary_salience(q3, k, 2), 1.0 / 6, rtol=0, atol=1e-15)
+
+
 def test_salience_zero_query_is_uniform():
     k = RNG.standard_normal((1, 2, 11, 4))
     s = oracle.salience(np.zeros_like(k), k)
