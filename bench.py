@@ -332,6 +332,20 @@ def e2e_throughput(wl, steps, warmup, stream, bytes_step):
     return bytes_step / dt / 1e9, h2d, d2h
 
 
+def summary_salience_measure(cs, steps, stream):
+    """Summary-row salience (CLIP CLS row) over the frames of `cs`: device
+    time per call (CUDA graph), and the algorithmic HBM bytes of one call."""
+    from visual_token_sparsity_gb300 import binding as sv, synth
+    q, k, _ = synth.draw_salience(cs, device="cuda")
+    sal = torch.empty(cs.batch, cs.N, device="cuda")
+    ws = sv.workspace(sv.sv_salience_summary_workspace_bytes(cs.batch, cs.H, cs.N, cs.d, 1))
+    fn = lambda: sv.sv_salience_summary(q, k, 1, 1 / math.sqrt(cs.d), sal, ws)
+    g = time_graph(fn, steps, 3, stream)
+    ms = replay_timed(g, steps, stream, lambda: None)
+    nbytes = cs.batch * cs.H * (cs.N + 1) * cs.d * 2 + cs.batch * cs.N * 4
+    return ms * 1e3, nbytes
+
+
 def salience_measure(batch, steps, warmup, stream, tiny=False):
     from visual_token_sparsity_gb300 import binding as sv, synth
     ss = synth.tiny_salience(batch=batch) if tiny else synth.siglip_salience(batch=batch)
@@ -555,6 +569,15 @@ def main():
                             "tflops": tf, "bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": tf / pk["bf16_tflops"], "peak_source": pk["source"],
                             "flop_count": "4*H*N^2*d per frame (both QK^T passes, d unpadded)"}
+    if not a.no_salience and a.workload != "tiny":
+        cs = synth.clip_summary_salience(batch=a.salience_batch)
+        us, nbytes = summary_salience_measure(cs, min(50, max(3, a.steps // 2)), stream)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        line["salience_summary"] = {
+            "workload": f"{cs.name}: {cs.batch} frames x {cs.N} tokens, {cs.H} heads, d {cs.d}, 1 summary row",
+            "us": us, "gbs": gbs, "bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"],
+            "bytes": "K once + the summary rows of Q + the fp32 salience"}
     if rank == 0:
         if world == 1 and not a.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(shape)

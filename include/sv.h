@@ -129,6 +129,27 @@ sv_status sv_salience_prefill(const void* q, const void* k, int B, int H, int N,
                               void* stream);
 
 /*
+ * Query-agnostic salience for encoders with summary tokens -- velog.io
+ * summary §3.1 encoder-type table: one summary token (CLIP), a token's
+ * importance is the attention it contributes to the summary token; several
+ * (RADIO), the mean attention toward them.  The R summary tokens are the
+ * first R tokens of the sequence:
+ *
+ *   salience[b][j] = 1/(H*R) * sum_h sum_{r<R} softmax_j(scale * q[b,h,r,:] . k[b,h,j,:])
+ *
+ * (softmax over all N tokens; summary columns are reported too).
+ * q, k     : bf16 [B][H][N][d], contiguous (only rows r < R of q are read).
+ * R        : 1 <= R <= min(16, N); R * N logits per head must fit in shared
+ *            memory (R * N <= ~56K).  d: a multiple of 8, at most 256.
+ * salience : out fp32 [B][N]; each row sums to 1.
+ * Only R rows of each head's attention map are formed: one CTA per (frame,
+ * head) streams K once (HBM-bound), then a head-mean kernel.  Deterministic.
+ */
+size_t sv_salience_summary_workspace_bytes(int B, int H, int N, int d, int R);
+sv_status sv_salience_summary(const void* q, const void* k, int B, int H, int N, int d, int R,
+                              float scale, float* salience, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Row-wise top-k (the selection step shared by prefill pruning and decode
  * retrieval) -- velog.io summary §3.1 (drop the lowest-salience tokens) and
  * §3.2 (activate the highest-scoring tokens); xllm-io review §五 topk.

@@ -66,6 +66,8 @@ _SIGS = {
                           _VP, _SZ, _VP]),
     "sv_pack_kv": (_I, [ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch), _VP, _I,
                         ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch), _VP, _SZ, _VP]),
+    "sv_salience_summary_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "sv_salience_summary": (_I, [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _SZ, _VP]),
     "sv_read_device_status": (_I, [_VP, _I, ctypes.POINTER(ctypes.c_int32), _VP]),
 }
 EXPORTED = tuple(_SIGS)
@@ -191,6 +193,20 @@ def sv_salience_prefill(q, k, scale, salience, ws, stream=None):
     B, H, N, d = q.shape
     assert k.shape == q.shape and salience.shape == (B, N)
     _check(lib.sv_salience_prefill(_ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), B, H, N, d,
+                                   float(scale), _ptr(salience, torch.float32, "salience"), *_ws(ws),
+                                   _stream(stream)))
+
+
+def sv_salience_summary_workspace_bytes(B, H, N, d, R):
+    return load().sv_salience_summary_workspace_bytes(B, H, N, d, R)
+
+
+def sv_salience_summary(q, k, R, scale, salience, ws, stream=None):
+    """q, k: bf16 [B][H][N][d] (summary tokens first); salience: fp32 [B][N] (written)."""
+    lib = load()
+    B, H, N, d = q.shape
+    assert k.shape == q.shape and salience.shape == (B, N)
+    _check(lib.sv_salience_summary(_ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), B, H, N, d, int(R),
                                    float(scale), _ptr(salience, torch.float32, "salience"), *_ws(ws),
                                    _stream(stream)))
 

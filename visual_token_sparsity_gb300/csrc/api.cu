@@ -161,6 +161,33 @@ sv_status sv_salience_prefill(const void* q, const void* k, int B, int H, int N,
   return cuda_status(e, "sv_salience_prefill");
 }
 
+size_t sv_salience_summary_workspace_bytes(int B, int H, int N, int d, int R) {
+  (void)d;
+  (void)R;
+  if (B < 0 || H < 0 || N < 0) return kStatusBytes;
+  return kStatusBytes + round256((size_t)B * H * N * sizeof(float));
+}
+
+sv_status sv_salience_summary(const void* q, const void* k, int B, int H, int N, int d, int R, float scale,
+                              float* salience, void* ws, size_t ws_bytes, void* stream) {
+  if (!q || !k || !salience) return fail(SV_ERR_INVALID_ARG, "q, k and salience must be non-NULL");
+  if (B < 0 || H <= 0 || N <= 0) return fail(SV_ERR_INVALID_ARG, "need B >= 0, H > 0, N > 0");
+  if (R < 1 || R > 16 || R > N) return fail(SV_ERR_INVALID_ARG, "need 1 <= R <= min(16, N) (R = %d)", R);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (d < 8 || d > 256 || d % 8) return fail(SV_ERR_UNSUPPORTED, "summary salience head_dim %d (multiple of 8, <= 256)", d);
+  if (!aligned16(q) || !aligned16(k)) return fail(SV_ERR_INVALID_ARG, "q and k must be 16-byte aligned");
+  if (sv::summary_smem_bytes(N, d, R) > kMaxSmemPerBlock - 4096)
+    return fail(SV_ERR_UNSUPPORTED, "R * N = %d logits do not fit in shared memory", R * N);
+  if ((long long)B * H > 0x7fffffffLL) return fail(SV_ERR_INVALID_ARG, "B * H too large");
+  sv_status s = check_ws(ws, ws_bytes, sv_salience_summary_workspace_bytes(B, H, N, d, R));
+  if (s != SV_OK) return s;
+  if (B == 0) return SV_OK;
+  cudaError_t e = sv::launch_summary_salience(q, k, B, H, N, d, R, scale, salience,
+                                              reinterpret_cast<float*>(after_status(ws)),
+                                              static_cast<cudaStream_t>(stream));
+  return cuda_status(e, "sv_salience_summary");
+}
+
 sv_status sv_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx, void* ws,
                        size_t ws_bytes, void* stream) {
   if (!scores || !idx) return fail(SV_ERR_INVALID_ARG, "scores and idx must be non-NULL");

@@ -142,7 +142,7 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
   // Row ids of a block of 128 tokens (8 sub-tiles) are resolved together, the
   // next block's while the current one streams: the index and page-table
   // loads cost two dependent round trips per block, not per sub-tile.
-  uint32_t blk_cur[4], blk_next[4];
+  uint32_t blk_cur[4] = {kNoRowM, kNoRowM, kNoRowM, kNoRowM}, blk_next[4] = {kNoRowM, kNoRowM, kNoRowM, kNoRowM};
   auto resolve_block = [&](int t0, uint32_t* r) {
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {

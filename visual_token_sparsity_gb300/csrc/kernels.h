@@ -77,6 +77,12 @@ cudaError_t launch_kv_append(void* k_pool, void* v_pool, int num_blocks, int Hkv
                              cudaStream_t stream);
 
 // ---- prefill salience (salience.cu)
+cudaError_t launch_head_mean(const float* colsum, int B, int H, int N, float inv, float* out,
+                             cudaStream_t stream);
+// ---- summary-row salience (summary.cu)
+size_t summary_smem_bytes(int N, int d, int R);
+cudaError_t launch_summary_salience(const void* q, const void* k, int B, int H, int N, int d, int R,
+                                    float scale, float* salience, float* colsum, cudaStream_t stream);
 size_t salience_workspace_bytes(int B, int H, int N, int d);
 cudaError_t launch_salience(const void* q, const void* k, int B, int H, int N, int d, float scale,
                             float* salience, void* ws, int* status, int num_sms,

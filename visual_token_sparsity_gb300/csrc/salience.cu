@@ -422,18 +422,6 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
   }
 }
 
-// s[b][j] = (1 / (H N)) * sum_h colsum[b][h][j], heads summed in order.
-__global__ void salience_head_mean_kernel(const float* __restrict__ colsum, int B, int H, int N,
-                                          float inv, float* __restrict__ out) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)B * N) return;
-  const long long b = i / N, j = i % N;
-  const float* p = colsum + b * H * (long long)N + j;
-  float s = 0.f;
-  for (int h = 0; h < H; ++h) s += p[(long long)h * N];
-  out[i] = s * inv;
-}
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -465,6 +453,27 @@ bool make_map(CUtensorMap* map, const void* base, int d, int N, int units) {
 }
 
 }  // namespace
+
+// s[b][j] = inv * sum_h colsum[b][h][j], heads summed in order (inv = 1 / (H N)
+// for the full salience, 1 / (H R) for the summary-row salience).
+__global__ void salience_head_mean_kernel(const float* __restrict__ colsum, int B, int H, int N,
+                                          float inv, float* __restrict__ out) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)B * N) return;
+  const long long b = i / N, j = i % N;
+  const float* p = colsum + b * H * (long long)N + j;
+  float s = 0.f;
+  for (int h = 0; h < H; ++h) s += p[(long long)h * N];
+  out[i] = s * inv;
+}
+
+cudaError_t launch_head_mean(const float* colsum, int B, int H, int N, float inv, float* out,
+                             cudaStream_t stream) {
+  const long long total = (long long)B * N;
+  if (total == 0) return cudaSuccess;
+  salience_head_mean_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(colsum, B, H, N, inv, out);
+  return cudaGetLastError();
+}
 
 size_t salience_smem_bytes(int N, int d) { return launch_smem(sal_geom(N, d)); }
 
@@ -500,10 +509,7 @@ cudaError_t launch_salience(const void* q, const void* k, int B, int H, int N, i
   salience_colsum_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long total = (long long)B * N;
-  salience_head_mean_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(
-      a.colsum, B, H, N, 1.0f / ((float)H * (float)N), salience);
-  return cudaGetLastError();
+  return launch_head_mean(a.colsum, B, H, N, 1.0f / ((float)H * (float)N), salience, stream);
 }
 
 }  // namespace sv

@@ -169,6 +169,13 @@ def siglip_salience(batch=256, keep=0.25):
                          C=1152, std=1.0 / math.sqrt(72.0), seed=2)
 
 
+def clip_summary_salience(batch=256, keep=0.25):
+    """CLIP ViT-L/14-336 encoder: 577 tokens (CLS + 24 x 24 patches), 16 heads,
+    d 64, 1024-wide features; salience from the CLS row (one summary token)."""
+    return SalienceShape("clip-vit-l-336-summary-salience", H=16, N=577, d=64, batch=batch, keep=keep,
+                         C=1024, std=1.0 / math.sqrt(64.0), seed=6)
+
+
 def longvila_decode(batch=1, layers=28):
     """Qwen2-7B attention (28 q heads, 4 KV heads, d 128), 256x196 visual + 256 text."""
     return DecodeShape("longvila-7b-decode", H=28, Hkv=4, d=128, n_vis=50176, n_text=256,
