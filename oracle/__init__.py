@@ -29,6 +29,7 @@ from .sparsevila import (  # noqa: F401
     summary_salience,
     topk_ascending,
     prune_compact,
+    prune_threshold,
     paged_view,
     retrieval_scores,
     retrieve_topk,

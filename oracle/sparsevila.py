@@ -127,6 +127,25 @@ def prune_compact(sal, feat, k):
     return idx, out
 
 
+def prune_threshold(sal, feat, threshold):
+    """Prefill prune by a salience threshold (a variable count per frame).
+
+    xllm-io review §五 query_agnostic_pruning: tokens whose salience exceeds
+    the threshold are kept (strictly greater), in their original order, and
+    their rows are gathered.
+
+    sal: [B][N]; feat: [B][N][C].  Returns a list over frames of
+    (kept indices ascending, kept rows [count][C]).
+    """
+    sal = np.asarray(sal)
+    feat = np.asarray(feat)
+    out = []
+    for b in range(sal.shape[0]):
+        idx = np.array([j for j in range(sal.shape[1]) if sal[b, j] > threshold], dtype=np.int64)
+        out.append((idx, feat[b, idx]))
+    return out
+
+
 def paged_view(pool, block_table, n_tokens):
     """Logical [B][Hkv][n_tokens][d] view of one layer's paged pool.
 

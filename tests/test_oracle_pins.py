@@ -330,6 +330,31 @@ def test_pack_order_and_head_map_by_token_id_encoding():
     np.testing.assert_array_equal(Vp, -Kp)
 
 
+def test_threshold_prune_extremes_and_strictness():
+    sal = np.array([[0.1, 0.3, 0.3, 0.05, 0.25]])
+    feat = np.arange(5 * 2, dtype=np.float64).reshape(1, 5, 2)
+    (idx, rows), = oracle.prune_threshold(sal, feat, -np.inf)
+    assert list(idx) == [0, 1, 2, 3, 4] and (rows == feat[0]).all()
+    (idx, rows), = oracle.prune_threshold(sal, feat, 0.3)            # equal to the threshold: dropped
+    assert len(idx) == 0 and rows.shape == (0, 2)
+    (idx, rows), = oracle.prune_threshold(sal, feat, 0.25)
+    assert list(idx) == [1, 2] and (rows == feat[0, [1, 2]]).all()
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_threshold_prune_between_ranks_equals_topk(seed):
+    rng = np.random.default_rng(seed)
+    sal = rng.standard_normal((3, 40))
+    feat = rng.standard_normal((3, 40, 4))
+    for k in (1, 7, 39):
+        srt = np.sort(sal, axis=1)[:, ::-1]
+        for b in range(3):
+            thr = 0.5 * (srt[b, k - 1] + srt[b, k])                  # between the k-th and (k+1)-th
+            (idx, rows), = oracle.prune_threshold(sal[b:b + 1], feat[b:b + 1], thr)
+            np.testing.assert_array_equal(idx, oracle.topk_ascending(sal[b:b + 1], k)[0])
+            np.testing.assert_array_equal(rows, feat[b, idx])
+
+
 def test_dense_attention_over_packed_equals_sparse_attention():
     B, H, Hkv, n_vis, n_text, d = 2, 6, 2, 20, 5, 8
     K = RNG.standard_normal((B, Hkv, n_vis + n_text, d))
