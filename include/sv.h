@@ -177,6 +177,24 @@ sv_status sv_prune_compact(const float* salience, int B, int N, int k, const voi
                            size_t ws_bytes, void* stream);
 
 /*
+ * Prefill prune by a salience threshold -- xllm-io review §五
+ * query_agnostic_pruning (keep the tokens whose salience exceeds the
+ * threshold): a variable number of tokens per frame.
+ *
+ * salience   : fp32 [B][N]; a token is kept iff salience > threshold
+ *              (strictly; NaN scores are dropped; a NaN threshold is an error).
+ * feat       : [B][N][row_bytes] opaque rows (row_bytes a multiple of 16; 0 = no rows).
+ * feat_out   : out [B][N][row_bytes]: rows [0, kept_count[b]) of frame b hold
+ *              the kept rows in token order; later rows are not written.
+ * kept_idx   : out int32 [B][N]: the kept indices ascending, then -1.
+ * kept_count : out device int32 [B].
+ * ws         : sv_prune_workspace_bytes(B, N, 1) (the status word).
+ */
+sv_status sv_prune_threshold(const float* salience, int B, int N, float threshold, const void* feat,
+                             int64_t row_bytes, void* feat_out, int32_t* kept_idx, int32_t* kept_count,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Decode query-aware retrieval -- velog.io summary §3.2 "Query-Aware Token
  * Selection" (text query as Query, cached visual tokens as Keys, aggregate
  * attention strength; the rest stays cached but inactive); xllm-io review §三

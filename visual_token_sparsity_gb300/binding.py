@@ -68,6 +68,7 @@ _SIGS = {
                         ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch), _VP, _SZ, _VP]),
     "sv_salience_summary_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "sv_salience_summary": (_I, [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _SZ, _VP]),
+    "sv_prune_threshold": (_I, [_VP, _I, _I, ctypes.c_float, _VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "sv_read_device_status": (_I, [_VP, _I, ctypes.POINTER(ctypes.c_int32), _VP]),
 }
 EXPORTED = tuple(_SIGS)
@@ -209,6 +210,18 @@ def sv_salience_summary(q, k, R, scale, salience, ws, stream=None):
     _check(lib.sv_salience_summary(_ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), B, H, N, d, int(R),
                                    float(scale), _ptr(salience, torch.float32, "salience"), *_ws(ws),
                                    _stream(stream)))
+
+
+def sv_prune_threshold(salience, threshold, feat, feat_out, kept_idx, kept_count, ws, stream=None):
+    """salience fp32 [B][N]; feat / feat_out [B][N][...] rows (or None); kept_idx int32 [B][N];
+    kept_count int32 [B] (device)."""
+    lib = load()
+    B, N = salience.shape
+    row_bytes = 0 if feat is None else feat.shape[2] * feat.element_size()
+    _check(lib.sv_prune_threshold(_ptr(salience, torch.float32, "salience"), B, N, float(threshold),
+                                  _ptr(feat, None, "feat"), row_bytes, _ptr(feat_out, None, "feat_out"),
+                                  _ptr(kept_idx, torch.int32, "kept_idx"), _ptr(kept_count, torch.int32, "kept_count"),
+                                  *_ws(ws), _stream(stream)))
 
 
 def sv_topk_rows(scores, k, idx, ws, stream=None):

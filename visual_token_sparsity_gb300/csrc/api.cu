@@ -203,6 +203,27 @@ sv_status sv_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx
   return cuda_status(e, "sv_topk_rows");
 }
 
+sv_status sv_prune_threshold(const float* salience, int B, int N, float threshold, const void* feat,
+                             int64_t row_bytes, void* feat_out, int32_t* kept_idx, int32_t* kept_count,
+                             void* ws, size_t ws_bytes, void* stream) {
+  if (!salience || !kept_idx || !kept_count)
+    return fail(SV_ERR_INVALID_ARG, "salience, kept_idx and kept_count must be non-NULL");
+  if (B < 0 || N <= 0 || N > (1 << 24)) return fail(SV_ERR_INVALID_ARG, "need B >= 0, 0 < N <= 2^24");
+  if (std::isnan(threshold)) return fail(SV_ERR_INVALID_ARG, "threshold is NaN");
+  if (row_bytes < 0 || row_bytes % 16) return fail(SV_ERR_INVALID_ARG, "row_bytes must be a multiple of 16");
+  if (row_bytes > 0 && (!feat || !feat_out)) return fail(SV_ERR_INVALID_ARG, "feat and feat_out must be non-NULL");
+  if (row_bytes > 0 && (!aligned16(feat) || !aligned16(feat_out)))
+    return fail(SV_ERR_INVALID_ARG, "feat and feat_out must be 16-byte aligned");
+  sv_status s = check_ws(ws, ws_bytes, sv_prune_workspace_bytes(B, N, 1));
+  if (s != SV_OK) return s;
+  if (B == 0) return SV_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = sv::launch_threshold_select(salience, B, N, threshold, kept_idx, kept_count, st);
+  if (e == cudaSuccess && row_bytes > 0)
+    e = sv::launch_gather_rows(feat, B, N, N, row_bytes, kept_idx, feat_out, status_word(ws), st, kept_count);
+  return cuda_status(e, "sv_prune_threshold");
+}
+
 sv_status sv_prune_compact(const float* salience, int B, int N, int k, const void* feat,
                            int64_t row_bytes, void* feat_out, int32_t* kept_idx, void* ws,
                            size_t ws_bytes, void* stream) {

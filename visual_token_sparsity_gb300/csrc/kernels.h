@@ -64,7 +64,10 @@ cudaError_t launch_sparse_attn_mma(const AttnArgs& a, const AttnPlan& p, cudaStr
 
 // ---- compaction gather (prune.cu)
 cudaError_t launch_gather_rows(const void* feat, int B, int N, int k, int64_t row_bytes,
-                               const int32_t* idx, void* out, int* status, cudaStream_t stream);
+                               const int32_t* idx, void* out, int* status, cudaStream_t stream,
+                               const int32_t* counts = nullptr);
+cudaError_t launch_threshold_select(const float* sal, int B, int N, float threshold, int32_t* idx, int32_t* count,
+                                    cudaStream_t stream);
 
 // ---- cache maintenance (evict.cu)
 cudaError_t launch_kv_move_down(void* k_pool, void* v_pool, int num_blocks, int Hkv, int D,
