@@ -33,6 +33,7 @@ from .sparsevila import (  # noqa: F401
     paged_view,
     retrieval_scores,
     retrieve_topk,
+    retrieval_scores_softmax,
     sparse_decode_attention,
     pack_selected_kv,
     evict_qa_tokens,

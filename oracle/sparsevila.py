@@ -200,6 +200,44 @@ def retrieve_topk(q, k_vis, k):
     return topk_ascending(sc, k), sc
 
 
+def retrieval_scores_softmax(q, K, n_vis, n_text, scale=None, lse=None):
+    """Softmax-normalised query-aware relevance of every cached visual token.
+
+    velog.io summary §3.2 "Query-Aware Token Selection": the aggregated
+    attention strength between the question's rows (Query) and the cached
+    vision tokens (Key); the retrieval kernel there runs alongside the
+    question's FlashAttention-2 prefill.  Reading taken for this variant:
+    the attention probability of each question row and query head to visual
+    token j, normalised over every cached token (visual and text, no causal
+    mask), summed over the rows and the heads that share the KV head.  When
+    ``lse`` is given (a caller's own prefill attention statistics, natural
+    log, [B][R][H]) it is used as each row's normaliser instead.
+
+    q: [B][R][H][d]; K: logical [B][Hkv][>= n_vis + n_text][d].
+    Returns [B][Hkv][n_vis].
+    """
+    q = _as_f64(q)
+    K = _as_f64(K)
+    B, R, H, d = q.shape
+    Hkv = K.shape[1]
+    G = H // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = np.zeros((B, Hkv, n_vis), dtype=np.float64)
+    for b in range(B):
+        for g in range(Hkv):
+            for r in range(R):
+                for h in range(g * G, (g + 1) * G):
+                    z = scale * (K[b, g, :n_vis + n_text] @ q[b, r, h])
+                    if lse is None:
+                        m = z.max()
+                        norm = m + math.log(np.exp(z - m).sum())
+                    else:
+                        norm = float(lse[b, r, h])
+                    out[b, g] += np.exp(z[:n_vis] - norm)
+    return out
+
+
 def sparse_decode_attention(q, K, V, vis_idx, n_vis, n_text, scale=None):
     """Decode attention over the retrieved visual tokens plus all text tokens.
 

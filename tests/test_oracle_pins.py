@@ -243,6 +243,42 @@ def _sdpa(q, K, V, scale):
     return out[:, :, 0, :].numpy()
 
 
+def test_softmax_retrieval_is_torch_softmax_mass_summed_over_rows_and_heads():
+    B, R, H, Hkv, nv, nt, d = 2, 3, 4, 2, 11, 5, 8
+    q = RNG.standard_normal((B, R, H, d))
+    K = RNG.standard_normal((B, Hkv, nv + nt, d))
+    got = oracle.retrieval_scores_softmax(q, K, nv, nt)
+    Kt = torch.from_numpy(K).repeat_interleave(H // Hkv, dim=1)       # [B][H][n][d]
+    p = torch.softmax(torch.einsum("brhd,bhnd->brhn", torch.from_numpy(q), Kt) / math.sqrt(d), dim=-1)
+    ref = p[..., :nv].sum(dim=1).view(B, Hkv, H // Hkv, nv).sum(dim=2).numpy()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
+
+
+def test_softmax_retrieval_mass_bounds_and_given_lse():
+    B, R, H, Hkv, nv, nt, d = 1, 2, 6, 3, 9, 4, 4
+    q = RNG.standard_normal((B, R, H, d))
+    K = RNG.standard_normal((B, Hkv, nv + nt, d))
+    sc = oracle.retrieval_scores_softmax(q, K, nv, nt)
+    sc0 = oracle.retrieval_scores_softmax(q, K[:, :, :nv], nv, 0)       # no text: all mass is visual
+    np.testing.assert_allclose(sc0.sum(-1), R * (H // Hkv), rtol=0, atol=1e-12)
+    assert (sc.sum(-1) < sc0.sum(-1)).all()
+    Kt = torch.from_numpy(K).repeat_interleave(H // Hkv, dim=1)
+    lse = torch.logsumexp(torch.einsum("brhd,bhnd->brhn", torch.from_numpy(q), Kt) / math.sqrt(d), dim=-1).numpy()
+    np.testing.assert_allclose(oracle.retrieval_scores_softmax(q, K, nv, nt, lse=lse), sc, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(oracle.retrieval_scores_softmax(q, K, nv, nt, lse=lse + 1.0), sc * math.exp(-1.0),
+                               rtol=1e-12, atol=0)
+
+
+def test_softmax_retrieval_one_row_one_head_ranks_like_dot_product():
+    q = RNG.standard_normal((1, 1, 2, 6))
+    K = RNG.standard_normal((1, 2, 30, 6))
+    sm = oracle.retrieval_scores_softmax(q, K, 25, 5)
+    raw = oracle.retrieval_scores(q, K[:, :, :25])
+    for k in (1, 5, 24):
+        np.testing.assert_array_equal(oracle.topk_ascending(sm.reshape(2, 25), k),
+                                      oracle.topk_ascending(raw.reshape(2, 25), k))
+
+
 def test_attention_all_tokens_equals_sdpa():
     B, H, Hkv, d, nv, nt = 2, 6, 2, 16, 30, 7
     q = RNG.standard_normal((B, H, d))
