@@ -642,6 +642,33 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
             "note": "attention over the retrieval's selection; pack once per round (all layers), "
                     "then dense attention over the packed pages each decode step"}
         del g_pack, g_dense
+    if not a.no_packed:
+        # softmax-normalised retrieval for a 32-row question (once per round)
+        from visual_token_sparsity_gb300 import binding as sv, synth
+        s = shape
+        R = 32
+        q32 = synth.normal_bf16((s.batch, R, s.H, s.d), synth.subseed(s.seed, 200, 1), device=dev)
+        lse32 = torch.zeros(s.batch, R, s.H, device=dev)
+        ws_s = sv.workspace(sv.sv_retrieve_softmax_workspace_bytes(s.batch, R, s.H, s.Hkv, s.d, s.n_vis, s.n_text), dev)
+        ws_d = sv.workspace(sv.sv_retrieve_workspace_bytes(s.batch, s.H, s.Hkv, s.d, s.n_vis, s.k), dev)
+        vis_s = torch.empty(s.batch, s.Hkv, s.k, dtype=torch.int32, device=dev)
+        soft = lambda: [sv.sv_retrieve_topk_softmax(q32, wl.scale, wl.layers[l], wl.seqs, s.k, vis_s, None, ws_s)
+                        for l in range(s.layers)]
+        fused = lambda: [sv.sv_retrieve_topk_softmax(q32, wl.scale, wl.layers[l], wl.seqs, s.k, vis_s, None, ws_s,
+                                                     lse=lse32) for l in range(s.layers)]
+        dot = lambda: [sv.sv_retrieve_topk(q32, wl.layers[l], wl.seqs, s.k, vis_s, None, ws_d) for l in range(s.layers)]
+        res = {}
+        for name, fn in (("softmax_us_per_layer", soft), ("softmax_given_lse_us_per_layer", fused),
+                         ("dot_us_per_layer", dot)):
+            g = time_graph(fn, max(3, a.steps // 4), 3, stream)
+            res[name] = replay_timed(g, max(3, a.steps // 4), stream, barrier) * 1e3 / s.layers
+            del g
+        kv = s.batch * s.Hkv * s.d * 2
+        res["question_rows"] = R
+        res["softmax_gbs"] = kv * (2 * s.n_vis + s.n_text) / (res["softmax_us_per_layer"] * 1e-6) / 1e9
+        res["note"] = ("per layer, once per round: the question's 32 rows score the visual tokens by attention "
+                       "mass (two passes over K, or one with the caller's prefill lse) vs the dot product")
+        line["retrieval_softmax"] = res
     del wl, g_step, g_attn
     torch.cuda.empty_cache()
 

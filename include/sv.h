@@ -245,6 +245,31 @@ sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const sv_kv_laye
                                    void* stream);
 
 /*
+ * Softmax-normalised query-aware retrieval -- velog.io summary §3.2
+ * ("aggregated attention strength" between the question's rows and the
+ * cached vision tokens; the pages' retrieval runs alongside the question's
+ * FlashAttention-2 prefill).  Per sequence b and KV head g:
+ *
+ *   score[b][g][j] = sum_{r<R} sum_{h in g} exp(scale * q[b,r,h] . K[b,g,j] - lse[b,r,h]),  j < n_vis
+ *   vis_idx[b][g]  = the k largest scores, ascending (ties -> lower index)
+ *
+ * lse : optional fp32 [B][R][H], natural log: each question row's softmax
+ *       normaliser from the caller's own prefill attention (the fused form;
+ *       no extra pass).  NULL: computed here over all n_vis + n_text cached
+ *       tokens, no causal mask (one extra pass over K).
+ * q   : bf16 [B][R][H][d]; R * (H / n_kv_heads) <= 256; d in {64, 128}.
+ * scores (optional out fp32 [B][Hkv][n_vis]), vis_idx, ws as sv_retrieve_topk;
+ * ws_bytes >= sv_retrieve_softmax_workspace_bytes(...).
+ * The logits are warp-level tensor-core tiles over the question rows of
+ * each KV head; deterministic.
+ */
+size_t sv_retrieve_softmax_workspace_bytes(int B, int R, int H, int n_kv_heads, int head_dim, int n_vis,
+                                           int n_text);
+sv_status sv_retrieve_topk_softmax(const void* q, int R, int H, float scale, const sv_kv_layer* layer,
+                                   const sv_seq_batch* seqs, const float* lse, int k, int32_t* vis_idx,
+                                   float* scores, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Sparse decode attention -- velog.io summary §3.2 (only the query-relevant
  * subset of the preserved visual cache is read) and §4.5 kernel table
  * ("decoding attention": reduced KV, less memory traffic).

@@ -16,6 +16,12 @@ Tolerances (stated once, used everywhere):
   by at most n * 6e-8 (4.4e-5 for n = 729) and typically sqrt(n) * 6e-8.
 * Retrieval scores (fp32 GEMV of d <= 128 terms): max |gpu - ref| <=
   1e-5 * max |ref| + 1e-6.
+* Softmax-normalised retrieval scores (sums over <= 256 question rows of
+  exp(z - lse), fp32 tensor-core logits of bf16 inputs, fp32 lse): per entry
+  |gpu - ref| <= 1e-4 |ref| + 1e-7 max|ref|.  The logits carry < 1e-6
+  absolute error (fp32 accumulation of d <= 128 exact products of size
+  < 64), which is the relative error of each exp; ex2 adds ~2e-7 and the
+  row sums ~R*G*6e-8.
 * Selected index sets: bit-exact except where scores tie within the band
   delta = 1e-3 * max(|tau|, rms(scores)) around the oracle's k-th score tau;
   the GPU set must have k distinct ascending indices, contain every j with
@@ -33,6 +39,7 @@ LSE_ABS = 1e-3
 SAL_REL = 1e-4
 SAL_SUM = 1e-5
 SCORE_REL = 1e-5
+SOFTMAX_SCORE_REL = 1e-4
 TIE_REL = 1e-3
 
 
@@ -86,3 +93,12 @@ def assert_scores_close(got, ref, what="scores"):
     err = np.abs(got - ref).max()
     bound = SCORE_REL * np.abs(ref).max() + 1e-6
     assert err <= bound, f"{what}: max err {err:.3g} > {bound:.3g}"
+
+
+def assert_softmax_scores_close(got, ref, what="softmax retrieval scores"):
+    got = _f64(got)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = SOFTMAX_SCORE_REL * np.abs(ref) + 1e-7 * np.abs(ref).max()
+    err = np.abs(got - ref)
+    i = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), f"{what}: |err| {err[i]:.3g} at ref {ref[i]:.3g} exceeds the bound {bound[i]:.3g}"

@@ -69,6 +69,9 @@ _SIGS = {
     "sv_salience_summary_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "sv_salience_summary": (_I, [_VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP, _VP, _SZ, _VP]),
     "sv_prune_threshold": (_I, [_VP, _I, _I, ctypes.c_float, _VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "sv_retrieve_softmax_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "sv_retrieve_topk_softmax": (_I, [_VP, _I, _I, ctypes.c_float, ctypes.POINTER(sv_kv_layer),
+                                      ctypes.POINTER(sv_seq_batch), _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
     "sv_read_device_status": (_I, [_VP, _I, ctypes.POINTER(ctypes.c_int32), _VP]),
 }
 EXPORTED = tuple(_SIGS)
@@ -250,6 +253,20 @@ def sv_retrieve_topk(q, layer, seqs, k, vis_idx, scores, ws, stream=None):
     _check(lib.sv_retrieve_topk(_ptr(q, torch.bfloat16, "q"), R, H, ctypes.byref(layer.c),
                                 ctypes.byref(seqs.c), k, _ptr(vis_idx, torch.int32, "vis_idx"),
                                 _ptr(scores, torch.float32, "scores"), *_ws(ws), _stream(stream)))
+
+
+def sv_retrieve_softmax_workspace_bytes(B, R, H, n_kv_heads, head_dim, n_vis, n_text):
+    return load().sv_retrieve_softmax_workspace_bytes(B, R, H, n_kv_heads, head_dim, n_vis, n_text)
+
+
+def sv_retrieve_topk_softmax(q, scale, layer, seqs, k, vis_idx, scores, ws, lse=None, stream=None):
+    """q bf16 [B][R][H][d]; lse fp32 [B][R][H] (natural log) or None; vis_idx int32 [B][Hkv][k]."""
+    lib = load()
+    B, R, H, d = q.shape
+    _check(lib.sv_retrieve_topk_softmax(_ptr(q, torch.bfloat16, "q"), R, H, float(scale), ctypes.byref(layer.c),
+                                        ctypes.byref(seqs.c), _ptr(lse, torch.float32, "lse"), int(k),
+                                        _ptr(vis_idx, torch.int32, "vis_idx"), _ptr(scores, torch.float32, "scores"),
+                                        *_ws(ws), _stream(stream)))
 
 
 def sv_retrieve_topk_noalloc(q, layer, seqs, k, vis_idx, scores=None, stream=None):

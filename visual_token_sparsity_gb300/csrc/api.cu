@@ -269,6 +269,38 @@ sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer
   return cuda_status(e, "sv_retrieve_topk");
 }
 
+size_t sv_retrieve_softmax_workspace_bytes(int B, int R, int H, int n_kv_heads, int head_dim, int n_vis,
+                                           int n_text) {
+  if (B < 0 || R <= 0 || H <= 0 || n_kv_heads <= 0 || H % n_kv_heads || n_vis < 0 || n_text < 0) return kStatusBytes;
+  return kStatusBytes + sv::retrieve_softmax_workspace_bytes(B, R, H, n_kv_heads, head_dim, n_vis, n_text);
+}
+
+sv_status sv_retrieve_topk_softmax(const void* q, int R, int H, float scale, const sv_kv_layer* layer,
+                                   const sv_seq_batch* seqs, const float* lse, int k, int32_t* vis_idx,
+                                   float* scores, void* ws, size_t ws_bytes, void* stream) {
+  sv_status s = check_cache(layer, seqs, false);
+  if (s != SV_OK) return s;
+  if (!q || !vis_idx) return fail(SV_ERR_INVALID_ARG, "q and vis_idx must be non-NULL");
+  if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  const int Hkv = layer->n_kv_heads;
+  if (R <= 0 || H <= 0 || H % Hkv) return fail(SV_ERR_INVALID_ARG, "need R > 0 and H a multiple of n_kv_heads");
+  if (R * (H / Hkv) > sv::retrieve_softmax_max_rows())
+    return fail(SV_ERR_UNSUPPORTED, "R * (H / n_kv_heads) = %d > %d question rows per KV head", R * (H / Hkv),
+                sv::retrieve_softmax_max_rows());
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (seqs->n_vis <= 0) return fail(SV_ERR_INVALID_ARG, "no visual tokens to retrieve from");
+  if (k < 1 || k > seqs->n_vis) return fail(SV_ERR_INVALID_ARG, "need 1 <= k <= n_vis (k = %d)", k);
+  s = check_ws(ws, ws_bytes,
+               sv_retrieve_softmax_workspace_bytes(seqs->batch, R, H, Hkv, layer->head_dim, seqs->n_vis, seqs->n_text));
+  if (s != SV_OK) return s;
+  if (seqs->batch == 0) return SV_OK;
+  cudaError_t e = sv::launch_retrieve_softmax(q, R, H, scale, layer->k_pool, layer->num_blocks, Hkv, layer->head_dim,
+                                              seqs->block_table, seqs->max_blocks, seqs->n_vis, seqs->n_text,
+                                              seqs->batch, lse, k, vis_idx, scores, after_status(ws), status_word(ws),
+                                              static_cast<cudaStream_t>(stream));
+  return cuda_status(e, "sv_retrieve_topk_softmax");
+}
+
 sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
                                 const sv_seq_batch* seqs, const int32_t* vis_idx, int k, void* out,
                                 float* lse, void* ws, size_t ws_bytes, void* stream) {

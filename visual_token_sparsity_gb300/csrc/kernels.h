@@ -15,6 +15,15 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
                             int batch, float* scores, int* status, int num_sms, int* row_done, int k,
                             int32_t* vis_idx, cudaStream_t stream);
 
+// ---- softmax-normalised retrieval (retrieve_softmax.cu): scores of visual
+// tokens = attention mass of the R x G question rows, then the row top-k
+size_t retrieve_softmax_workspace_bytes(int B, int R, int H, int Hkv, int D, int n_vis, int n_text);
+int retrieve_softmax_max_rows();
+cudaError_t launch_retrieve_softmax(const void* q, int R, int H, float scale, const void* k_pool, int num_blocks,
+                                    int Hkv, int D, const int32_t* block_table, int max_blocks, int n_vis,
+                                    int n_text, int batch, const float* lse_in, int k, int32_t* vis_idx,
+                                    float* scores_out, void* ws, int* status, cudaStream_t stream);
+
 // ---- row top-k (topk.cu: one CTA per row; topk_cluster.cu: an 8-CTA cluster
 // per row for long rows)
 cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
