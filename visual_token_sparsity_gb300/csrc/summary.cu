@@ -19,7 +19,11 @@
 namespace sv {
 
 namespace {
-constexpr int kSumThreads = 256;
+// 128 threads: more independent CTAs per SM overlap one CTA's load phase with
+// another's row reductions (measured faster than 256 or 512; batching more
+// than four token groups per lane costs occupancy, and staging the head's K
+// through one bulk copy into shared memory was slower)
+constexpr int kSumThreads = 128;
 constexpr int kSumWarps = kSumThreads / 32;
 
 size_t summary_smem(int N, int d, int R) { return ((size_t)R * d + (size_t)R * N + 2 * (size_t)R) * sizeof(float); }
