@@ -75,6 +75,13 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   // fill, partial write)
   const long long min_tokens = attn_uses_mma(G) ? (units >= 16 ? 256 : 128) : 0;
   if (tpw * p.tile < min_tokens) tpw = (min_tokens + p.tile - 1) / p.tile;
+  // CUDA-core path: stay within the fused merge (at most kFusedMergeMaxSplits
+  // splits, merged by the last warp) when that still leaves 512 or more warps;
+  // a separate merge launch costs more than longer splits at small batches
+  if (!attn_uses_mma(G) && (tiles + tpw - 1) / tpw > kFusedMergeMaxSplits) {
+    const long long tpw2 = (tiles + kFusedMergeMaxSplits - 1) / kFusedMergeMaxSplits;
+    if (units * ((tiles + tpw2 - 1) / tpw2) >= 512) tpw = tpw2;
+  }
   p.chunk = (int)(tpw * p.tile);
   p.nsplit = n_tokens > 0 ? (n_tokens + p.chunk - 1) / p.chunk : 1;
   // nsplit <= ceil(tiles / tpw) <= min(tiles, ceil(target / units), max): a
