@@ -12,19 +12,21 @@
 // units; 16 softmax warps, one MMA-issue warp and one TMA warp.  Per unit two
 // passes run back to back over 128-row tiles x 128-column chunks:
 //   pass 1  K_h resident in shared memory, 128-row tiles of Q_h streamed by
-//           TMA; S = Q_tile K_chunk^T (M=128, N<=128, K=d padded to 16) goes
-//           to one of four 128-column TMEM buffers; every softmax thread owns
-//           one query row (one TMEM lane) of the chunk and keeps an online
-//           max / sum of exp2 (log2 domain); per tile the four partial
-//           log-sum-exps of a row are merged into lse_i in shared memory.
+//           TMA; S = Q_tile K_chunk^T (M=128, N<=256, K=d padded to 16) goes
+//           to one of two 256-column TMEM buffers; every softmax thread owns
+//           one query row (one TMEM lane) of a 64-column slice of the chunk
+//           and keeps an online max / sum of exp2 (log2 domain); per tile the
+//           four slice log-sum-exps of a row are merged into lse_i in shared
+//           memory.
 //   pass 2  Q_h resident, 128-row tiles of K_h streamed; S^T = K_tile Q^T puts
 //           one key per TMEM lane, so the column sum over queries becomes a
 //           per-thread row sum of exp2(z - lse_i) with lse_i broadcast from
 //           shared memory.  Padded queries carry lse = +inf and contribute 0.
-// Chunk u of the whole sequence goes to TMEM buffer u % 4 and is consumed by
-// the four warps (one per TMEM lane quarter) of part u % 4, so the four warps
-// that share an SM sub-partition work on different chunks at different times
-// and keep the exp unit busy through each other's TMEM-load latency.
+// Chunk u of the whole sequence goes to TMEM buffer u % 2; all 16 softmax
+// warps read every chunk (warp w: lane quarter w % 4, slice w / 4), so while
+// they work through one buffer the MMAs refill the other, and no warp waits
+// for the refill of "its" buffer.  One N=256 MMA costs about as much as one
+// N=128 MMA here, so the 256-column chunks halve the tensor-pipe time.
 // The resident operand is replaced chunk by chunk: as soon as the last tile's
 // MMAs on a 128-row chunk complete, the TMA warp loads the next pass's (or the
 // next unit's) rows there, so the tensor pipe never drains between passes.
@@ -34,8 +36,9 @@
 // uses packed fp32x2 FMA/ADD, a 3-input max tree, a stale running max
 // (rescaled only when it grows by more than 8), one 32-column group in
 // registers at a time and one accumulator chain; variants with
-// double-buffered TMEM loads, more accumulator chains, scalar arithmetic or
-// 256-column buffers measured slower on the SigLIP shape.
+// double-buffered TMEM loads, more accumulator chains, scalar arithmetic,
+// 24 softmax warps or buffers tied to warps measured slower on the SigLIP
+// shape.
 // Shared-memory operands use the K-major no-swizzle layout (8x16-byte core
 // matrices); TMA writes them directly with 8-element x 128-row boxes, and out
 // of range rows are zero-filled by TMA.  Head dims that are not a multiple of
@@ -52,17 +55,17 @@ namespace sv {
 namespace {
 
 // Work split (chosen by measurement on the SigLIP shape; see the notes at the
-// top): four 128-column TMEM buffers, each chunk consumed by one softmax warp
-// per lane quarter, 32-column groups loaded one at a time and summed into one
-// fp32x2 accumulator.  The code also handles wider buffers (kBufCols = 256
-// with several warps per buffer quarter), which measured slower.
-constexpr int kBufs = 4;                       // TMEM buffers (one chunk each)
-constexpr int kBufCols = 128;                  // columns of one TMEM buffer (N of one MMA)
+// top): two 256-column TMEM buffers filled by N=256 MMAs; every softmax warp
+// reads a fixed 64-column slice of every chunk, 32-column groups loaded one
+// at a time and summed into one fp32x2 accumulator.
+constexpr int kBufs = 2;                       // TMEM buffers (one chunk each)
+constexpr int kBufCols = 256;                  // columns of one TMEM buffer (N of one MMA)
 constexpr int kPieces = kBufCols / 128;        // 128-row resident pieces per chunk
-constexpr int kHalves = 1;                     // softmax warps sharing a buffer's lane quarter
-constexpr int kWarpCols = (kBufCols / kHalves + 31) / 32 * 32;  // chunk columns per softmax warp (last may get fewer)
-constexpr int kParts = kBufs * kHalves;        // softmax warps per TMEM lane quarter
-constexpr int kSoftWarps = 4 * kParts;
+constexpr int kSlices = 4;                     // softmax warps per TMEM lane quarter
+constexpr int kWarpCols = kBufCols / kSlices;  // columns of every chunk per softmax warp
+static_assert(kWarpCols % 32 == 0, "slices are whole 32-column groups");
+constexpr int kParts = kSlices;                // row partials per lane (one per slice)
+constexpr int kSoftWarps = 4 * kSlices;
 constexpr int kSlots = 2;        // streamed 128-row operand tiles in flight
 constexpr int kMmaWarp = kSoftWarps, kTmaWarp = kSoftWarps + 1;
 constexpr int kThreads = (kSoftWarps + 2) * 32;
@@ -182,7 +185,7 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
     }
     for (int i = 0; i < kBufs; ++i) {
       ptx::mbar_init(&sh.bar_full[i], 1);
-      ptx::mbar_init(&sh.bar_empty[i], 4 * kHalves);  // the buffer's softmax warps
+      ptx::mbar_init(&sh.bar_empty[i], kSoftWarps);  // every softmax warp reads every chunk
     }
     for (int i = 0; i < nt; ++i) {
       ptx::mbar_init(&sh.bar_res[i], 1);
@@ -283,37 +286,47 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
   } else {
     // ------------------------------------------------ softmax warps
     // warp w reads TMEM lane quarter (w & 3) -- the hardware ties a warp to the
-    // lanes 32 * (w % 4) .. + 31 -- and part p = w >> 2 takes the chunks u
-    // with u % 4 == p % 4, columns [(p / 4) * kWarpCols, + kWarpCols) of each.
-    const int quarter = warp & 3, part = warp >> 2, buf = part % kBufs, half = part / kBufs;
+    // lanes 32 * (w % 4) .. + 31 -- and its slice p = w >> 2 is the columns
+    // [p * kWarpCols, + kWarpCols) of every chunk, whichever buffer holds it.
+    const int quarter = warp & 3, part = warp >> 2;
     const int row = quarter * 32 + lane;
-    const int col_lo = half * kWarpCols;
-    const int my_cols = max(0, min(kWarpCols, kBufCols - col_lo));
+    const int col_lo = part * kWarpCols;
+    const int my_cols = kWarpCols;
     const int nch = (a.Np + kBufCols - 1) / kBufCols;
-    const uint32_t taddr = tbase + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kBufCols + col_lo);
+    const uint32_t tlane = tbase + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col_lo;
     const float sl2 = a.sl2;
     const uint64_t sl2x2 = fm::splat2(sl2);
     float* my_part = part_lse + part * Rr;
     uint32_t u = 0;
     uint32_t v[32];
-    // Runs fn(column offset) on each of the ng 32-column groups at TMEM
-    // address ta, the group's values in v.  One group at a time: a single
-    // compact loop body measured faster than double-buffered loads.
+    // Runs fn(column offset) on each of the ng <= 2 32-column groups of the
+    // warp's slice at TMEM address ta, the group's values in v.  One group
+    // in registers at a time, straight-line: loading the second group while
+    // the first is summed, or releasing the buffer before the last group's
+    // arithmetic, measured slower.
+    static_assert(kWarpCols <= 64, "a slice is at most two groups");
     auto for_groups = [&](uint32_t ta, int ng, auto&& fn) {
-      for (int gi = 0; gi < ng; ++gi) {
-        ptx::tmem_ld32(ta + 32 * gi, v);
+      if (ng > 0) {
+        ptx::tmem_ld32(ta, v);
         ptx::tmem_wait_ld(v);
-        fn(32 * gi);
+        fn(0);
+      }
+      if (ng > 1) {
+        ptx::tmem_ld32(ta + 32, v);
+        ptx::tmem_wait_ld(v);
+        fn(32);
       }
     };
+    // chunk u sits in buffer u % kBufs
     auto chunk_begin = [&]() {
-      wait_bar(&sh.bar_full[buf], (u / kBufs) & 1, sh);
+      wait_bar(&sh.bar_full[u % kBufs], (u / kBufs) & 1, sh);
       ptx::tc_fence_after();
+      return tlane + (u % kBufs) * kBufCols;
     };
     auto chunk_end = [&]() {
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[buf]);
+      if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[u % kBufs]);
     };
     for (int unit = blockIdx.x; unit < a.units; unit += gridDim.x) {
       // pass 1: per-part row log-sum-exp (log2 domain)
@@ -321,8 +334,7 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         const bool live = t * kTileRows + quarter * 32 < a.N;
         float m = -INFINITY, l = 0.f;
         for (int c = 0; c < nch; ++c, ++u) {
-          if ((int)(u % kBufs) != buf) continue;
-          chunk_begin();
+          const uint32_t taddr = chunk_begin();
           const int nc = min(my_cols, a.Np - kBufCols * c - col_lo);
           for_groups(taddr, live && nc > 0 ? nc >> 5 : 0, [&](int g) {
             const int key0 = kBufCols * c + col_lo + g;
@@ -385,17 +397,21 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         const bool live = t * kTileRows + quarter * 32 < a.N;
         uint64_t acc = 0;
         for (int c = 0; c < nch; ++c, ++u) {
-          if ((int)(u % kBufs) != buf) continue;
-          chunk_begin();
+          const uint32_t taddr = chunk_begin();
           const int nc = min(my_cols, a.Np - kBufCols * c - col_lo);
           for_groups(taddr, live && nc > 0 ? nc >> 5 : 0, [&](int g) {
-            // lse of the group's 32 queries: the same for every lane (broadcast)
-            const uint64_t* nl = reinterpret_cast<const uint64_t*>(nlse2 + kBufCols * c + col_lo + g);
+            // lse of the group's 32 queries: the same for every lane (broadcast
+            // 16-byte loads; the offset is a multiple of 32 floats)
+            const ulonglong2* nl = reinterpret_cast<const ulonglong2*>(nlse2 + kBufCols * c + col_lo + g);
 #pragma unroll
-            for (int pr = 0; pr < 16; ++pr) {
-              const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
-                                          sl2x2, nl[pr]);
-              acc = fm::add2(acc, fm::exp2_mufu2(x));
+            for (int pq = 0; pq < 8; ++pq) {
+              const ulonglong2 w = nl[pq];
+              const uint64_t x0 = fm::fma2(fm::pack2(__uint_as_float(v[4 * pq]), __uint_as_float(v[4 * pq + 1])),
+                                           sl2x2, w.x);
+              acc = fm::add2(acc, fm::exp2_mufu2(x0));
+              const uint64_t x1 = fm::fma2(fm::pack2(__uint_as_float(v[4 * pq + 2]), __uint_as_float(v[4 * pq + 3])),
+                                           sl2x2, w.y);
+              acc = fm::add2(acc, fm::exp2_mufu2(x1));
             }
           });
           chunk_end();
