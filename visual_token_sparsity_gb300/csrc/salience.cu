@@ -332,7 +332,8 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
       // pass 1: per-part row log-sum-exp (log2 domain)
       for (int t = 0; t < nt; ++t) {
         const bool live = t * kTileRows + quarter * 32 < a.N;
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY;
+        uint64_t l2 = 0;  // running sum of the row's exps, two halves
         for (int c = 0; c < nch; ++c, ++u) {
           const uint32_t taddr = chunk_begin();
           const int nc = min(my_cols, a.Np - kBufCols * c - col_lo);
@@ -355,26 +356,25 @@ salience_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             // stale running max: rescale only when the group max exceeds it by
             // more than 8 (log2 units), so the exps need not wait for the max
             const float cms = cm * sl2;
+            // (a group always holds a key below N, so m is finite after the
+            // first group and the exps below never see m = -inf)
             if (cms > m + 8.0f) {
-              l = l * fm::ex2_mufu(m - cms);
+              l2 = fm::mul2(l2, fm::splat2(fm::ex2_mufu(m - cms)));
               m = cms;
             }
-            if (m == -INFINITY) return;
             const uint64_t nmn = fm::splat2(-m);
-            uint64_t acc = 0;
 #pragma unroll
             for (int pr = 0; pr < 16; ++pr) {
               const uint64_t x = fm::fma2(fm::pack2(__uint_as_float(v[2 * pr]), __uint_as_float(v[2 * pr + 1])),
                                           sl2x2, nmn);
-              acc = fm::add2(acc, fm::exp2_mufu2(x));
+              l2 = fm::add2(l2, fm::exp2_mufu2(x));
             }
-            float s0, s1;
-            fm::unpack2(acc, s0, s1);
-            l += s0 + s1;
           });
           chunk_end();
         }
-        my_part[t * kTileRows + row] = m == -INFINITY ? -INFINITY : m + __log2f(l);
+        float l0, l1;
+        fm::unpack2(l2, l0, l1);
+        my_part[t * kTileRows + row] = m == -INFINITY ? -INFINITY : m + __log2f(l0 + l1);
       }
       softmax_bar();
       for (int r = threadIdx.x; r < Rr; r += kSoftWarps * 32) {
