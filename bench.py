@@ -59,6 +59,7 @@ def parse():
     p.add_argument("--no-decode", action="store_true", help="salience measurement only")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-packed", action="store_true", help="skip the pack-once KV comparison")
+    p.add_argument("--no-varlen", action="store_true", help="skip the per-sequence-length decode step")
     return p.parse_args()
 
 
@@ -179,6 +180,26 @@ def decode_bytes(shape):
     retrieve = shape.n_vis * shape.Hkv * d2                                # visual keys
     attend = (shape.k + shape.n_text) * shape.Hkv * d2 * 2 + shape.k * shape.Hkv * 4   # K+V + indices
     return shape.layers * shape.batch * retrieve, shape.layers * shape.batch * attend
+
+
+def varlen_counts(shape):
+    """Per-sequence (n_vis, n_text, k) of a threshold-pruned batch: a salience
+    threshold keeps a different share of each sequence's visual tokens, so
+    visual counts are drawn uniformly from [n_vis / 2, n_vis], text counts
+    from [n_text / 2, n_text], and each sequence selects floor(keep * n_vis_b)
+    (seeded; the batch-wide counts are the capacities)."""
+    rng = np.random.default_rng(shape.seed + 17)
+    nv = rng.integers(shape.n_vis // 2, shape.n_vis + 1, size=shape.batch)
+    nt = rng.integers(shape.n_text // 2, shape.n_text + 1, size=shape.batch)
+    k = np.floor(shape.keep * nv).astype(np.int64)
+    return [int(x) for x in nv], [int(x) for x in nt], [int(x) for x in k]
+
+
+def varlen_bytes(shape, nv, nt, k):
+    """Algorithmic HBM bytes of one decode step with per-sequence counts."""
+    d2 = shape.d * 2
+    per_seq = [v * shape.Hkv * d2 + (kk + t) * shape.Hkv * d2 * 2 + kk * shape.Hkv * 4 for v, t, kk in zip(nv, nt, k)]
+    return shape.layers * sum(per_seq)
 
 
 class DecodeWorkload:
@@ -669,6 +690,25 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
         res["note"] = ("per layer, once per round: the question's 32 rows score the visual tokens by attention "
                        "mass (two passes over K, or one with the caller's prefill lse) vs the dot product")
         line["retrieval_softmax"] = res
+    if not a.no_varlen:
+        # per-sequence lengths: the same cache read as a threshold-pruned
+        # batch, each sequence with its own visual, text and selected counts
+        from visual_token_sparsity_gb300 import binding as sv
+        nv, nt, kk = varlen_counts(shape)
+        arr = lambda x: torch.tensor(x, dtype=torch.int32, device=dev)
+        uniform = wl.seqs
+        wl.seqs = sv.SeqBatch(wl.bt, shape.n_vis, shape.n_text, arr(nv), arr(nt), arr(kk))
+        g_vl = time_graph(wl.step, a.steps, 3, stream)
+        ms_vl = replay_timed(g_vl, a.steps, stream, barrier)
+        wl.seqs = uniform
+        gbs = varlen_bytes(shape, nv, nt, kk) / (ms_vl * 1e-3) / 1e9
+        line["variable_lengths"] = {
+            "step_us": ms_vl * 1e3, "gbs": gbs, "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"],
+            "n_vis_range": [min(nv), max(nv)], "n_text_range": [min(nt), max(nt)], "k_range": [min(kk), max(kk)],
+            "tokens_vs_uniform": (sum(nv) + sum(nt)) / (shape.batch * (shape.n_vis + shape.n_text)),
+            "note": "retrieval + sparse attention per layer with per-sequence counts (sv_seq_batch n_vis_seq / "
+                    "n_text_seq / k_seq); GB/s of the per-sequence algorithmic bytes"}
+        del g_vl
     del wl, g_step, g_attn
     torch.cuda.empty_cache()
 

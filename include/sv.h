@@ -29,8 +29,9 @@
  *     (cudaGetLastError).  On an error nothing is launched and
  *     sv_last_error() returns a description (thread-local).
  *   - Device-side index errors (a block id outside the pool, a visual index
- *     outside [0, n_vis)) set a bit in the status word; the offending load is
- *     skipped (read as zero).  Kernels never trap.
+ *     outside [0, n_vis), a per-sequence length outside its capacity) set a
+ *     bit in the status word; the offending load (or sequence) is skipped.
+ *     Kernels never trap.
  *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16).  Accumulation is
  *     fp32.  No C++ exception crosses this ABI.
  *   - GQA: query head h reads KV head h / G with G = H / Hkv.
@@ -57,6 +58,7 @@ typedef enum {
 /* Device status bits (the status word is the first int32 of a workspace). */
 #define SV_DEV_BAD_BLOCK 0x1   /* a block-table entry outside [0, num_blocks) */
 #define SV_DEV_BAD_INDEX 0x2   /* a visual index outside [0, n_vis) */
+#define SV_DEV_BAD_LENGTH 0x4  /* a per-sequence length outside its capacity; that sequence is skipped */
 #define SV_DEV_TIMEOUT   0x10  /* a bounded wait inside a kernel gave up (2 s); results undefined */
 
 /* Tokens per KV page (fixed). */
@@ -86,7 +88,23 @@ typedef struct {
  * block_table: DEVICE int32 [batch][max_blocks]; logical position t of
  * sequence b lives in page block_table[b][t / 16], row t % 16.
  * Logical layout of every sequence: visual tokens at [0, n_vis), then n_text
- * text tokens.  Lengths are uniform over the batch.
+ * text tokens.
+ *
+ * Per-sequence lengths (xllm-io review §五: a threshold prune keeps a
+ * different number of visual tokens per frame or sequence).  The three
+ * optional DEVICE int32 [batch] arrays below give each sequence its own
+ * counts; NULL means the batch-wide value.  With any of them set, n_vis,
+ * n_text and the calls' k are CAPACITIES: every per-sequence count must lie
+ * in [0, capacity] (and k_seq[b] <= n_vis_seq[b]); score rows keep the stride
+ * n_vis, index rows the stride k, split plans and workspaces are sized for
+ * the capacities.  Sequence b's visual tokens sit at [0, n_vis_seq[b]) and
+ * its text right after them, at [n_vis_seq[b], n_vis_seq[b] + n_text_seq[b]).
+ * A sequence whose counts are out of range sets SV_DEV_BAD_LENGTH and is
+ * skipped (its indices read -1, its attention output 0).
+ * Accepted by sv_retrieve_topk, sv_retrieve_topk_noalloc,
+ * sv_sparse_decode_attn and sv_kv_append; the other calls taking a batch
+ * return SV_ERR_UNSUPPORTED when any of the arrays is set.
+ * Zero-initialise the struct so that the arrays default to NULL.
  */
 typedef struct {
   const int32_t* block_table;
@@ -94,6 +112,9 @@ typedef struct {
   int32_t max_blocks;
   int32_t n_vis;
   int32_t n_text;
+  const int32_t* n_vis_seq;   /* optional [batch]: visual tokens of each sequence */
+  const int32_t* n_text_seq;  /* optional [batch]: text tokens of each sequence */
+  const int32_t* k_seq;       /* optional [batch]: selected visual tokens of each sequence */
 } sv_seq_batch;
 
 /* ------------------------------------------------------------------------
@@ -204,9 +225,12 @@ sv_status sv_prune_threshold(const float* salience, int B, int N, float threshol
  *   vis_idx[b][g]  = top-k of score[b][g]  (ties -> lower index, ascending)
  *
  * q        : bf16 [B][R][H][d] (the current question's query rows).
- * layer    : the layer's paged cache; seqs: batch view (only n_vis is used).
- * vis_idx  : out int32 [B][Hkv][k].
- * scores   : optional out fp32 [B][Hkv][n_vis] (NULL = not written).
+ * layer    : the layer's paged cache; seqs: batch view (n_vis, or the
+ *            per-sequence n_vis_seq and k_seq).
+ * vis_idx  : out int32 [B][Hkv][k].  With k_seq, row (b, g) holds k_seq[b]
+ *            ascending indices and -1 in its remaining slots.
+ * scores   : optional out fp32 [B][Hkv][n_vis] (NULL = not written; with
+ *            n_vis_seq only the first n_vis_seq[b] entries of a row).
  * Supported: d in {64, 128}; 1 <= k <= n_vis; H % Hkv == 0.
  */
 sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer,
@@ -280,6 +304,10 @@ sv_status sv_retrieve_topk_softmax(const void* q, int R, int H, float scale, con
  * q       : bf16 [B][H][d] (one decode query per head).
  * vis_idx : int32 [B][Hkv][k], distinct values in [0, n_vis); NULL = all
  *           n_vis visual tokens (dense attention; k is then ignored).
+ *           Per-sequence lengths: sequence b attends to the first k_seq[b]
+ *           entries of its rows (values in [0, n_vis_seq[b])) and to its
+ *           n_text_seq[b] text tokens at [n_vis_seq[b], + n_text_seq[b]);
+ *           with vis_idx NULL, to all its n_vis_seq[b] visual tokens.
  * out     : out bf16 [B][H][d].
  * lse     : optional out fp32 [B][H], log sum_t exp(scale q.k_t) (NULL = none).
  * Split-K over tokens with an fp32 online softmax; per-split partials live in
@@ -337,6 +365,9 @@ sv_status sv_evict_qa_tokens(const sv_kv_layer* layers, int n_layers, sv_seq_bat
 /*
  * Append T new tokens' K/V at logical positions [n_vis + n_text, + T) of every
  * sequence (a helper for driving rounds; the caller then adds T to n_text).
+ * With per-sequence lengths: at [n_vis_seq[b] + n_text_seq[b], + T) of
+ * sequence b (the caller then adds T to each n_text_seq entry); n_vis +
+ * n_text + T must still fit in max_blocks * 16.
  * k_new, v_new: bf16 [B][T][Hkv][d].  The pages must already be in the table.
  */
 sv_status sv_kv_append(const sv_kv_layer* layer, const sv_seq_batch* seqs, const void* k_new,

@@ -19,6 +19,7 @@ _lib = None
 SV_OK = 0
 SV_DEV_BAD_BLOCK = 0x1
 SV_DEV_BAD_INDEX = 0x2
+SV_DEV_BAD_LENGTH = 0x4
 BLOCK_TOKENS = 16
 
 
@@ -37,7 +38,8 @@ class sv_kv_layer(ctypes.Structure):
 class sv_seq_batch(ctypes.Structure):
     _fields_ = [("block_table", ctypes.c_void_p), ("batch", ctypes.c_int32),
                 ("max_blocks", ctypes.c_int32), ("n_vis", ctypes.c_int32),
-                ("n_text", ctypes.c_int32)]
+                ("n_text", ctypes.c_int32), ("n_vis_seq", ctypes.c_void_p),
+                ("n_text_seq", ctypes.c_void_p), ("k_seq", ctypes.c_void_p)]
 
 
 _VP, _SZ, _I, _F, _I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float, ctypes.c_int64
@@ -143,12 +145,25 @@ class KvLayer:
 
 
 class SeqBatch:
-    """Block table (int32 [batch][max_blocks]) plus uniform lengths."""
+    """Block table (int32 [batch][max_blocks]) plus lengths: uniform n_vis /
+    n_text, or -- with the optional int32 [batch] device tensors n_vis_seq,
+    n_text_seq, k_seq -- per-sequence counts, n_vis / n_text then being the
+    capacities."""
 
-    def __init__(self, block_table, n_vis, n_text):
+    def __init__(self, block_table, n_vis, n_text, n_vis_seq=None, n_text_seq=None, k_seq=None):
         self.block_table = block_table
-        self.c = sv_seq_batch(_ptr(block_table, torch.int32, "block_table"), block_table.shape[0],
-                              block_table.shape[1], int(n_vis), int(n_text))
+        self.n_vis_seq, self.n_text_seq, self.k_seq = n_vis_seq, n_text_seq, k_seq
+        B = block_table.shape[0]
+
+        def opt(t, name):
+            if t is None:
+                return None
+            if t.shape != (B,):
+                raise ValueError(f"{name} must have shape ({B},), got {tuple(t.shape)}")
+            return _ptr(t, torch.int32, name)
+        self.c = sv_seq_batch(_ptr(block_table, torch.int32, "block_table"), B,
+                              block_table.shape[1], int(n_vis), int(n_text), opt(n_vis_seq, "n_vis_seq"),
+                              opt(n_text_seq, "n_text_seq"), opt(k_seq, "k_seq"))
 
     @property
     def n_vis(self):

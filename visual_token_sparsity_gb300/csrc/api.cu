@@ -76,6 +76,22 @@ sv_status check_cache(const sv_kv_layer* L, const sv_seq_batch* S, bool need_v) 
   return SV_OK;
 }
 
+// Per-sequence lengths of a batch view (all NULL: uniform lengths).
+sv::SeqLens lens_of(const sv_seq_batch* S) {
+  sv::SeqLens l;
+  l.n_vis = S->n_vis_seq;
+  l.n_text = S->n_text_seq;
+  l.k = S->k_seq;
+  return l;
+}
+
+sv_status reject_lens(const sv_seq_batch* S, const char* call) {
+  if (S && lens_of(S).any())
+    return fail(SV_ERR_UNSUPPORTED, "%s: per-sequence lengths (n_vis_seq / n_text_seq / k_seq) are not supported",
+                call);
+  return SV_OK;
+}
+
 }  // namespace
 
 namespace sv {
@@ -265,7 +281,8 @@ sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer
   float* sc = scores ? scores : reinterpret_cast<float*>(after_status(ws) + round256(rows * sizeof(int)));
   cudaError_t e = sv::launch_retrieve(q, R, H, H / Hkv, layer->k_pool, layer->num_blocks, Hkv,
                                       layer->head_dim, seqs->block_table, seqs->max_blocks, seqs->n_vis,
-                                      seqs->batch, sc, status_word(ws), num_sms(), row_done, k, vis_idx, st);
+                                      seqs->batch, sc, status_word(ws), num_sms(), row_done, k, vis_idx, st,
+                                      lens_of(seqs), seqs->n_text);
   return cuda_status(e, "sv_retrieve_topk");
 }
 
@@ -279,6 +296,8 @@ sv_status sv_retrieve_topk_softmax(const void* q, int R, int H, float scale, con
                                    const sv_seq_batch* seqs, const float* lse, int k, int32_t* vis_idx,
                                    float* scores, void* ws, size_t ws_bytes, void* stream) {
   sv_status s = check_cache(layer, seqs, false);
+  if (s != SV_OK) return s;
+  s = reject_lens(seqs, "sv_retrieve_topk_softmax");
   if (s != SV_OK) return s;
   if (!q || !vis_idx) return fail(SV_ERR_INVALID_ARG, "q and vis_idx must be non-NULL");
   if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q must be 16-byte aligned");
@@ -328,6 +347,7 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
   a.block_table = seqs->block_table; a.max_blocks = seqs->max_blocks;
   a.vis_idx = vis_idx; a.k_vis = k_vis; a.n_vis = seqs->n_vis; a.n_text = seqs->n_text;
   a.batch = seqs->batch; a.out = out; a.lse = lse;
+  a.lens = lens_of(seqs);
   // the counters' offset depends only on the batch shape, so a workspace
   // reused with other token counts finds them where the last call zeroed them
   const size_t cnt_bytes = round256((size_t)seqs->batch * Hkv * sizeof(int));
@@ -346,6 +366,9 @@ sv_status sv_pack_kv(const sv_kv_layer* src, const sv_seq_batch* seqs, const int
   sv_status s = check_cache(src, seqs, true);
   if (s != SV_OK) return s;
   s = check_cache(dst, dst_seqs, true);
+  if (s != SV_OK) return s;
+  s = reject_lens(seqs, "sv_pack_kv");
+  if (s == SV_OK) s = reject_lens(dst_seqs, "sv_pack_kv");
   if (s != SV_OK) return s;
   if (dst->n_kv_heads != src->n_kv_heads || dst->head_dim != src->head_dim)
     return fail(SV_ERR_INVALID_ARG, "source and packed layers differ in n_kv_heads or head_dim");
@@ -370,6 +393,7 @@ sv_status sv_evict_qa_tokens(const sv_kv_layer* layers, int n_layers, sv_seq_bat
                              int32_t text_begin, int32_t text_end, int32_t* n_blocks_in_use,
                              void* ws, size_t ws_bytes, void* stream) {
   if (!layers || !seqs || n_layers < 0) return fail(SV_ERR_INVALID_ARG, "layers and seqs must be non-NULL");
+  if (reject_lens(seqs, "sv_evict_qa_tokens") != SV_OK) return SV_ERR_UNSUPPORTED;
   if (text_begin < 0 || text_begin > text_end || text_end > seqs->n_text)
     return fail(SV_ERR_INVALID_ARG, "need 0 <= text_begin <= text_end <= n_text (%d, %d, %d)",
                 text_begin, text_end, seqs->n_text);
@@ -414,7 +438,8 @@ sv_status sv_kv_append(const sv_kv_layer* layer, const sv_seq_batch* seqs, const
                                           layer->n_kv_heads, layer->head_dim, seqs->block_table,
                                           seqs->max_blocks, seqs->batch, seqs->n_vis + seqs->n_text,
                                           k_new, v_new, T, status_word(ws),
-                                          static_cast<cudaStream_t>(stream)),
+                                          static_cast<cudaStream_t>(stream), lens_of(seqs), seqs->n_vis,
+                                          seqs->n_text),
                      "sv_kv_append");
 }
 

@@ -108,7 +108,8 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
                          int max_blocks, const int32_t* __restrict__ vis_idx, int k_vis,
                          int n_vis, int n_text, float scale_log2, int batch, int nsplit, int chunk,
                          float* __restrict__ part_ml, float* __restrict__ part_o, int* status,
-                         int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse) {
+                         int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse,
+                         SeqLens lens) {
   using S = AttnShape<D, G>;
   constexpr int LPT = S::LPT, TPI = S::TPI, TILE = S::TILE, NL = S::NL, DUP = S::DUP;
 
@@ -118,7 +119,12 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   const int split = (int)(w % nsplit);
   const int bg = (int)(w / nsplit);
   const int b = bg / Hkv, g = bg % Hkv;
-  const int T = k_vis + n_text;
+  // this sequence's counts (k_vis, n_vis, n_text are capacities with
+  // per-sequence lengths; splits past its tokens stay empty)
+  int nv, nt, kb;
+  attn_lengths(lens, vis_idx != nullptr, b, n_vis, n_text, k_vis, lane == 0 && split == 0 && g == 0, status,
+               nv, nt, kb);
+  const int T = kb + nt;
   const int t_begin = split * chunk;
   const int t_end = min(T, t_begin + chunk);
   const int dim0 = (lane % LPT) * 8;
@@ -156,9 +162,9 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   auto load_pos = [&](int t0) -> int {
     const int tok = t0 + lane;
     if (lane >= TILE || tok >= t_end) return -1;
-    if (tok >= k_vis) return n_vis + (tok - k_vis);
+    if (tok >= kb) return nv + (tok - kb);
     const int pos = vrow ? __ldg(vrow + tok) : tok;
-    if (pos < 0 || pos >= n_vis) { flag_status(status, kStatusBadIndex); return -1; }
+    if (pos < 0 || pos >= nv) { flag_status(status, kStatusBadIndex); return -1; }
     return pos;
   };
   auto lookup = [&](int pos) -> uint32_t {
@@ -311,7 +317,7 @@ static void launch_split(const AttnArgs& a, const AttnPlan& p, cudaStream_t stre
       static_cast<const uint16_t*>(a.q), a.H, static_cast<const uint16_t*>(a.k_pool),
       static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks,
       a.vis_idx, a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk,
-      a.part_ml, a.part_o, a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse);
+      a.part_ml, a.part_o, a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse, a.lens);
 }
 
 template <int D>

@@ -69,7 +69,8 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
                        int max_blocks, const int32_t* __restrict__ vis_idx, int k_vis, int n_vis,
                        int n_text, float scale_log2, int batch, int nsplit, int chunk,
                        float* __restrict__ part_ml, float* __restrict__ part_o, int* status,
-                       int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse) {
+                       int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse,
+                       SeqLens lens) {
   constexpr int CPR = D / 8;                         // 16-byte chunks per token row
   constexpr int KSTEPS = D / 16;
   constexpr int NT_O = D / 8;                        // output n-tiles (8 dims each)
@@ -84,7 +85,11 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
   const int split = (int)(w % nsplit);
   const int bg = (int)(w / nsplit);
   const int b = bg / Hkv, g = bg % Hkv;
-  const int T = k_vis + n_text;
+  // this sequence's counts (capacities with per-sequence lengths)
+  int nv, nt, kb;
+  attn_lengths(lens, vis_idx != nullptr, b, n_vis, n_text, k_vis, lane == 0 && split == 0 && g == 0, status,
+               nv, nt, kb);
+  const int T = kb + nt;
   const int t_begin = split * chunk;
   const int t_end = min(T, t_begin + chunk);
   const int32_t* bt = block_table + (size_t)b * max_blocks;
@@ -149,11 +154,11 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
       const int tok = t0 + 32 * q4 + lane;
       int pos = -1;
       if (tok < t_end) {
-        if (tok < k_vis) {
+        if (tok < kb) {
           pos = vrow ? __ldg(vrow + tok) : tok;
-          if (pos < 0 || pos >= n_vis) { flag_status(status, kStatusBadIndex); pos = -1; }
+          if (pos < 0 || pos >= nv) { flag_status(status, kStatusBadIndex); pos = -1; }
         } else {
-          pos = n_vis + (tok - k_vis);
+          pos = nv + (tok - kb);
         }
       }
       r[q4] = (uint32_t)pos;
@@ -364,7 +369,7 @@ cudaError_t launch_sparse_attn_mma(const AttnArgs& a, const AttnPlan& p, cudaStr
   static_cast<const uint16_t*>(a.q), a.H, G, static_cast<const uint16_t*>(a.k_pool),                        \
       static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks, a.vis_idx, \
       a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk, a.part_ml, a.part_o,       \
-      a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse
+      a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse, a.lens
   if (a.D == 128)
     sparse_attn_mma_kernel<128><<<grid, kMmaWarps * 32, smem, stream>>>(SV_MMA_ARGS);
   else

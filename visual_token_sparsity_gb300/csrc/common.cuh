@@ -4,15 +4,52 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 namespace sv {
 
 constexpr int kBlockTokens = 16;
 constexpr int kStatusBadBlock = 0x1;
 constexpr int kStatusBadIndex = 0x2;
+constexpr int kStatusBadLength = 0x4;  // a per-sequence length outside its capacity
 constexpr int kStatusTimeout = 0x10;   // a bounded wait inside a kernel gave up
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void flag_status(int* status, int bits) { atomicOr(status, bits); }
+
+// Sequence b's visual, text and selected counts under `s`, whose capacities
+// are n_vis, n_text and k.  False (counts set to 0) when a count lies outside
+// [0, its capacity] or the selection exceeds the visual count: the caller
+// skips the sequence and reports kStatusBadLength.
+__device__ __forceinline__ bool seq_lengths(const SeqLens& s, int b, int n_vis, int n_text, int k,
+                                            int& nv, int& nt, int& kb) {
+  nv = s.n_vis ? __ldg(s.n_vis + b) : n_vis;
+  nt = s.n_text ? __ldg(s.n_text + b) : n_text;
+  kb = s.k ? __ldg(s.k + b) : k;
+  if (nv < 0 || nv > n_vis || nt < 0 || nt > n_text || kb < 0 || kb > k || kb > nv) {
+    nv = nt = kb = 0;
+    return false;
+  }
+  return true;
+}
+
+// Attention token counts of sequence b: visual nv, text nt and attended
+// visual kb (the k_vis listed indices, or all nv visual tokens when there is
+// no index list).  Out-of-range lengths attend nothing; `report` selects the
+// one thread that sets kStatusBadLength.
+__device__ __forceinline__ void attn_lengths(const SeqLens& lens, bool indexed, int b, int n_vis,
+                                             int n_text, int k_vis, bool report, int* status, int& nv,
+                                             int& nt, int& kb) {
+  nv = n_vis;
+  nt = n_text;
+  kb = indexed ? k_vis : n_vis;
+  if (!lens.any()) return;
+  SeqLens l = lens;
+  if (!indexed) l.k = nullptr;
+  const bool ok = seq_lengths(l, b, n_vis, n_text, indexed ? k_vis : 0, nv, nt, kb);
+  if (!indexed) kb = nv;
+  if (!ok && report) flag_status(status, kStatusBadLength);
+}
 
 // Two bf16 values packed in a 32-bit word -> fp32 (exact).
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }

@@ -83,12 +83,15 @@ cudaError_t launch_kv_move_down(void* k_pool, void* v_pool, int num_blocks, int 
   return cudaGetLastError();
 }
 
-// Writes new tokens' K/V rows ([B][T][Hkv][d], token-major) into their pages.
+// Writes new tokens' K/V rows ([B][T][Hkv][d], token-major) into their pages,
+// at [pos0, pos0 + T) or, with per-sequence lengths, after each sequence's
+// own visual and text tokens (capacities n_vis, n_text keep every position
+// inside the block table).
 __global__ void __launch_bounds__(256)
 kv_append_kernel(uint4* k_pool, uint4* v_pool, int num_blocks, int Hkv, int vecs_per_tok,
                  const int32_t* __restrict__ block_table, int max_blocks, int pos0,
                  const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, int T,
-                 long long total, int* status) {
+                 long long total, int* status, SeqLens lens, int n_vis, int n_text) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int v = (int)(i % vecs_per_tok);
@@ -97,8 +100,19 @@ kv_append_kernel(uint4* k_pool, uint4* v_pool, int num_blocks, int Hkv, int vecs
     r /= Hkv;
     const int t = (int)(r % T);
     const int b = (int)(r / T);
+    int p0 = pos0;
+    if (lens.any()) {
+      SeqLens l = lens;
+      l.k = nullptr;
+      int nv, nt, kb;
+      if (!seq_lengths(l, b, n_vis, n_text, 0, nv, nt, kb)) {
+        if (v == 0 && g == 0 && t == 0) flag_status(status, kStatusBadLength);
+        continue;
+      }
+      p0 = nv + nt;
+    }
     const long long off = token_vec(block_table + (size_t)b * max_blocks, num_blocks, Hkv, g,
-                                    pos0 + t, vecs_per_tok, status);
+                                    p0 + t, vecs_per_tok, status);
     if (off < 0) continue;
     k_pool[off + v] = k_new[i];
     v_pool[off + v] = v_new[i];
@@ -108,7 +122,7 @@ kv_append_kernel(uint4* k_pool, uint4* v_pool, int num_blocks, int Hkv, int vecs
 cudaError_t launch_kv_append(void* k_pool, void* v_pool, int num_blocks, int Hkv, int D,
                              const int32_t* block_table, int max_blocks, int batch, int pos0,
                              const void* k_new, const void* v_new, int T, int* status,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const SeqLens& lens, int n_vis, int n_text) {
   const long long total = (long long)batch * T * Hkv * (D / 8);
   if (total == 0) return cudaSuccess;
   long long blocks = (total + 255) / 256;
@@ -116,7 +130,7 @@ cudaError_t launch_kv_append(void* k_pool, void* v_pool, int num_blocks, int Hkv
   kv_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
       static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), num_blocks, Hkv, D / 8,
       block_table, max_blocks, pos0, static_cast<const uint4*>(k_new),
-      static_cast<const uint4*>(v_new), T, total, status);
+      static_cast<const uint4*>(v_new), T, total, status, lens, n_vis, n_text);
   return cudaGetLastError();
 }
 

@@ -7,13 +7,27 @@
 
 namespace sv {
 
+// Optional per-sequence lengths of a decode batch: device int32 arrays of
+// `batch` entries, nullptr = the batch-wide value for every sequence.  With
+// any of them set, the batch-wide n_vis / n_text / k are capacities: strides
+// of the score and index arrays, workspace sizes and split plans.
+struct SeqLens {
+  const int32_t* n_vis = nullptr;   // visual tokens of each sequence
+  const int32_t* n_text = nullptr;  // text tokens of each sequence
+  const int32_t* k = nullptr;       // selected visual tokens of each sequence
+  __host__ __device__ bool any() const { return n_vis || n_text || k; }
+};
+
 // ---- retrieval scoring + top-k (retrieve.cu).  With row_done (zeroed int per
 // (sequence, KV head) row) and rows that fit in shared memory, the top-k runs
 // inside the scoring kernel; otherwise a separate top-k kernel follows.
+// Per-sequence lengths: scores of sequence b cover its n_vis[b] tokens, its
+// rows select k[b] indices and fill the rest of the k slots with -1.
 cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_pool, int num_blocks,
                             int Hkv, int D, const int32_t* block_table, int max_blocks, int n_vis,
                             int batch, float* scores, int* status, int num_sms, int* row_done, int k,
-                            int32_t* vis_idx, cudaStream_t stream);
+                            int32_t* vis_idx, cudaStream_t stream, const SeqLens& lens = SeqLens{},
+                            int n_text = 0);
 
 // ---- softmax-normalised retrieval (retrieve_softmax.cu): scores of visual
 // tokens = attention mass of the R x G question rows, then the row top-k
@@ -25,13 +39,17 @@ cudaError_t launch_retrieve_softmax(const void* q, int R, int H, float scale, co
                                     float* scores_out, void* ws, int* status, cudaStream_t stream);
 
 // ---- row top-k (topk.cu: one CTA per row; topk_cluster.cu: an 8-CTA cluster
-// per row for long rows)
+// per row for long rows).  n and k are the row stride of scores and idx; with
+// per-sequence lengths (rows_per_seq rows per sequence) row r uses
+// lens.n_vis / lens.k of sequence r / rows_per_seq and fills its slots past
+// that k with -1 (out-of-range lengths: the whole row is -1).
 cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const SeqLens& lens = SeqLens{}, int rows_per_seq = 1);
 bool topk_cluster_fits(int n);
 bool topk_prefers_cluster(int n);   // long rows that fit: use launch_topk_cluster
 cudaError_t launch_topk_cluster(const float* scores, int rows, int n, int k, int32_t* idx,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const SeqLens& lens = SeqLens{},
+                                int rows_per_seq = 1);
 
 // ---- pack-once KV (pack.cu): selected visual + text rows of src copied to
 // positions [0, k + n_text) of every sequence of dst (same Hkv and D)
@@ -60,7 +78,8 @@ struct AttnArgs {
   const int32_t* block_table;
   int max_blocks;
   const int32_t* vis_idx;
-  int k_vis, n_vis, n_text, batch;
+  int k_vis, n_vis, n_text, batch;   // capacities when lens has per-sequence counts
+  SeqLens lens;                       // vis_idx == nullptr: lens.k is ignored (all visual tokens)
   void* out;
   float* lse;
   float* part_ml;
@@ -83,10 +102,14 @@ cudaError_t launch_kv_move_down(void* k_pool, void* v_pool, int num_blocks, int 
                                 const int32_t* block_table, int max_blocks, int batch,
                                 int dst_pos, int src_pos, int count, int* status,
                                 cudaStream_t stream);
+// new tokens go to positions [pos0, pos0 + T); with per-sequence lengths
+// pos0 of sequence b is lens.n_vis[b] + lens.n_text[b] (each falling back to
+// n_vis / n_text), and pos0 is unused
 cudaError_t launch_kv_append(void* k_pool, void* v_pool, int num_blocks, int Hkv, int D,
                              const int32_t* block_table, int max_blocks, int batch, int pos0,
                              const void* k_new, const void* v_new, int T, int* status,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const SeqLens& lens = SeqLens{}, int n_vis = 0,
+                             int n_text = 0);
 
 // ---- prefill salience (salience.cu)
 cudaError_t launch_head_mean(const float* colsum, int B, int H, int N, float inv, float* out,

@@ -93,6 +93,10 @@ extern "C" sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const
                         "(use sv_retrieve_topk with a workspace)", n_scores, kMaxScores);
   if (seqs->batch == 0) return SV_OK;
 
+  sv::SeqLens lens;
+  lens.n_vis = seqs->n_vis_seq;
+  lens.n_text = seqs->n_text_seq;
+  lens.k = seqs->k_seq;
   void* base = nullptr;
   sv_status s = scratch_on_current_device(&base);
   if (s != SV_OK) return s;
@@ -106,7 +110,7 @@ extern "C" sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     e = sv::launch_retrieve(q, R, H, H / Hkv, layer->k_pool, layer->num_blocks, Hkv, layer->head_dim,
                             seqs->block_table, seqs->max_blocks, seqs->n_vis, seqs->batch, sc, status, sms,
-                            nullptr, k, vis_idx, st);
+                            nullptr, k, vis_idx, st, lens, seqs->n_text);
   }
   if (e != cudaSuccess) return noalloc_fail(SV_ERR_CUDA, "sv_retrieve_topk_noalloc: %s", cudaGetErrorString(e));
   return SV_OK;

@@ -44,7 +44,7 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
                       const uint16_t* __restrict__ k_pool, int num_blocks, int Hkv,
                       const int32_t* __restrict__ block_table, int max_blocks, int n_vis,
                       int blocks_per_cta, float* __restrict__ scores, int* status,
-                      int* row_done, int k, int32_t* __restrict__ vis_idx) {
+                      int* row_done, int k, int32_t* __restrict__ vis_idx, SeqLens lens, int n_text) {
   constexpr int LPT = D / 8;        // lanes per token row (16 B each)
   constexpr int TPI = 32 / LPT;     // tokens per warp-wide load
   constexpr int NL = kBlockTokens / TPI;  // loads per lane per page
@@ -62,7 +62,12 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
 
-  const int n_vblocks = (n_vis + kBlockTokens - 1) / kBlockTokens;
+  // this sequence's visual count and selection size (n_vis and k are the
+  // capacities: the strides of scores and vis_idx)
+  int nv = n_vis, nt, kb = k;
+  if (lens.any() && !seq_lengths(lens, b, n_vis, n_text, k, nv, nt, kb) && tid == 0 && blockIdx.x == 0)
+    flag_status(status, kStatusBadLength);
+  const int n_vblocks = (nv + kBlockTokens - 1) / kBlockTokens;
   const int blk_begin = blockIdx.x * blocks_per_cta;
   const int blk_end = min(n_vblocks, blk_begin + blocks_per_cta);
   const int32_t* bt = block_table + (size_t)b * max_blocks;
@@ -120,7 +125,7 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
     }
     GroupReduce<NL, LPT>::run(part, lane);
     const int pos = blk * kBlockTokens + my_tok;
-    if ((lane & 1) == 0 && pos < n_vis) out[pos] = part[0];
+    if ((lane & 1) == 0 && pos < nv) out[pos] = part[0];
     if (SV_RET_PREFETCH) {
 #pragma unroll
       for (int i = 0; i < NL; ++i) cur[i] = nxt[i];
@@ -135,7 +140,9 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  block_topk_row(out, n_vis, k, vis_idx + (size_t)row * k, topk_keys, ts);
+  int32_t* dst = vis_idx + (size_t)row * k;
+  if (kb > 0) block_topk_row(out, nv, kb, dst, topk_keys, ts);
+  fill_unselected(dst, kb, k);
   if (tid == 0) row_done[row] = 0;   // ready for the next call
 }
 
@@ -144,7 +151,7 @@ bool retrieve_fuses_topk(int n_vis) { return n_vis <= kFuseMaxN; }
 cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_pool, int num_blocks,
                             int Hkv, int D, const int32_t* block_table, int max_blocks, int n_vis,
                             int batch, float* scores, int* status, int num_sms, int* row_done, int k,
-                            int32_t* vis_idx, cudaStream_t stream) {
+                            int32_t* vis_idx, cudaStream_t stream, const SeqLens& lens, int n_text) {
   const int n_vblocks = (n_vis + kBlockTokens - 1) / kBlockTokens;
   const int rows = batch * Hkv;
   // about two waves of 8-warp CTAs over the GPU, at least one page per warp
@@ -163,15 +170,16 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
   if (D == 128)
     retrieve_score_kernel<128><<<grid, kRetrieveThreads, smem, stream>>>(
         qq, R, H, G, kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
-        vis_idx);
+        vis_idx, lens, n_text);
   else
     retrieve_score_kernel<64><<<grid, kRetrieveThreads, smem, stream>>>(
         qq, R, H, G, kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
-        vis_idx);
+        vis_idx, lens, n_text);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || fuse) return e;
-  if (topk_prefers_cluster(n_vis)) return launch_topk_cluster(scores, rows, n_vis, k, vis_idx, stream);
-  return launch_topk_rows(scores, rows, n_vis, k, vis_idx, stream);
+  if (topk_prefers_cluster(n_vis))
+    return launch_topk_cluster(scores, rows, n_vis, k, vis_idx, stream, lens, Hkv);
+  return launch_topk_rows(scores, rows, n_vis, k, vis_idx, stream, lens, Hkv);
 }
 
 }  // namespace sv

@@ -14,18 +14,21 @@ namespace sv {
 
 __global__ void __launch_bounds__(1024)
 topk_rows_kernel(const float* __restrict__ scores, int n, int k, int32_t* __restrict__ idx,
-                 int keys_in_smem) {
+                 int keys_in_smem, SeqLens lens, int rows_per_seq) {
   extern __shared__ uint32_t smem_keys[];
   __shared__ TopkShared ts;
   const int row = blockIdx.x;
-  block_topk_row(scores + (size_t)row * n, n, k, idx + (size_t)row * k,
-                 keys_in_smem ? smem_keys : nullptr, ts);
+  int nr = n, kr = k;
+  if (lens.any()) row_lengths(lens, row, rows_per_seq, n, k, nr, kr);
+  int32_t* dst = idx + (size_t)row * k;
+  if (kr > 0) block_topk_row(scores + (size_t)row * n, nr, kr, dst, keys_in_smem ? smem_keys : nullptr, ts);
+  fill_unselected(dst, kr, k);
 }
 
 int topk_max_smem_keys() { return 52 * 1024; }   // 208 KB of keys
 
 cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const SeqLens& lens, int rows_per_seq) {
   if (rows == 0) return cudaSuccess;
   const bool in_smem = n <= topk_max_smem_keys();
   const size_t smem = in_smem ? (size_t)n * sizeof(uint32_t) : 0;
@@ -40,7 +43,8 @@ cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  topk_rows_kernel<<<rows, threads, smem, stream>>>(scores, n, k, idx, in_smem ? 1 : 0);
+  topk_rows_kernel<<<rows, threads, smem, stream>>>(scores, n, k, idx, in_smem ? 1 : 0, lens,
+                                                    rows_per_seq > 0 ? rows_per_seq : 1);
   return cudaGetLastError();
 }
 

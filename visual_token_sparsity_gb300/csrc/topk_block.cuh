@@ -66,6 +66,23 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* warp_tmp) {
   return res;
 }
 
+// Row `row`'s key count nr and selection size kr under per-sequence lengths
+// (rows_per_seq rows per sequence; n and k are the capacities); (0, 0) when
+// a length is out of range.
+__device__ __forceinline__ void row_lengths(const SeqLens& lens, int row, int rows_per_seq, int n, int k,
+                                            int& nr, int& kr) {
+  SeqLens l = lens;
+  l.n_text = nullptr;
+  int nt;
+  seq_lengths(l, row / rows_per_seq, n, 0, k, nr, nt, kr);
+}
+
+// Index slots [from, k) of a row that selected fewer than k tokens get -1
+// (all threads of the block call this).
+__device__ __forceinline__ void fill_unselected(int32_t* dst, int from, int k) {
+  for (int i = from + (int)threadIdx.x; i < k; i += (int)blockDim.x) dst[i] = -1;
+}
+
 // All threads of the block call this.  keys: shared memory for n keys, or
 // nullptr to re-read `src` (through L2) on every pass.  `src` may have been
 // written by other CTAs of the running grid: it is read with ld.global.cg.

@@ -31,7 +31,8 @@ constexpr int kTopkClusterThreads = 512;
 }  // namespace
 
 __global__ void __cluster_dims__(kTopkClusterCtas, 1, 1) __launch_bounds__(kTopkClusterThreads)
-topk_cluster_kernel(const float* __restrict__ scores, int n, int k, int32_t* __restrict__ idx) {
+topk_cluster_kernel(const float* __restrict__ scores, int n_cap, int k_cap, int32_t* __restrict__ idx,
+                    SeqLens lens, int rows_per_seq) {
   extern __shared__ uint32_t keys[];
   __shared__ int hist[2][256];    // double-buffered: peers read pass p's while pass p+1 fills the other
   __shared__ int total[256];
@@ -44,10 +45,17 @@ topk_cluster_kernel(const float* __restrict__ scores, int n, int k, int32_t* __r
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  // this row's key count and selection size (the same for every CTA of the
+  // cluster, so an empty selection leaves the cluster together)
+  int n = n_cap, k = k_cap;
+  if (lens.any()) row_lengths(lens, row, rows_per_seq, n_cap, k_cap, n, k);
+  int32_t* dst = idx + (size_t)row * k_cap;
+  if (rank == 0) fill_unselected(dst, k, k_cap);
+  if (k <= 0) return;
   const int slice = (n + kTopkClusterCtas - 1) / kTopkClusterCtas;
   const int lo_i = min(n, rank * slice), hi_i = min(n, lo_i + slice);
   const int m = hi_i - lo_i;
-  const float* src = scores + (size_t)row * n + lo_i;
+  const float* src = scores + (size_t)row * n_cap + lo_i;
 
   // stage this CTA's keys (four independent loads in flight per thread) and
   // its smallest / largest key
@@ -195,7 +203,6 @@ topk_cluster_kernel(const float* __restrict__ scores, int n, int k, int32_t* __r
   take_eq = take_eq < 0 ? 0 : (take_eq > eq ? eq : take_eq);
   int o = gt_before + (int)(packed >> 16) + min(eq_before, remaining);
   int e = 0;
-  int32_t* dst = idx + (size_t)row * k;
   for (int i = s0; i < s1; ++i) {
     const uint32_t kp = keys[i] & pmask;
     bool take = kp > prefix;
@@ -218,7 +225,7 @@ bool topk_cluster_fits(int n) {
 bool topk_prefers_cluster(int n) { return n > 16384 && topk_cluster_fits(n); }
 
 cudaError_t launch_topk_cluster(const float* scores, int rows, int n, int k, int32_t* idx,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const SeqLens& lens, int rows_per_seq) {
   if (rows == 0) return cudaSuccess;
   const int slice = (n + kTopkClusterCtas - 1) / kTopkClusterCtas;
   const size_t smem = (size_t)slice * sizeof(uint32_t);
@@ -232,7 +239,8 @@ cudaError_t launch_topk_cluster(const float* scores, int rows, int n, int k, int
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   dim3 grid(kTopkClusterCtas, rows);
-  topk_cluster_kernel<<<grid, kTopkClusterThreads, smem, stream>>>(scores, n, k, idx);
+  topk_cluster_kernel<<<grid, kTopkClusterThreads, smem, stream>>>(scores, n, k, idx, lens,
+                                                                   rows_per_seq > 0 ? rows_per_seq : 1);
   return cudaGetLastError();
 }
 
