@@ -104,18 +104,9 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Same, with each descriptor given as its two 32-bit halves (the start
-// address sits in the low half, so stepping along a tile is one 32-bit add).
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, with each
+// shared-memory descriptor given as its two 32-bit halves (the start address
+// sits in the low half, so stepping along a tile is one 32-bit add).
 __device__ __forceinline__ void mma_bf16_split(uint32_t tmem_d, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -162,22 +153,13 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t* r) {
                : "memory");
 }
 
-// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
-// 8 rows x 16 bytes; `lbo` = byte distance between K-adjacent core matrices,
-// `sbo` = byte distance between 8-row groups.
-__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-  return d;                // base offset 0, absolute-LBO mode off, no swizzle
-}
-
-// Halves of smem_desc_kmajor: low = start address >> 4 | (lbo >> 4) << 16,
-// high = sbo >> 4 | version bit.  Shared-window addresses stay below 2^18,
-// so adding a multiple of 16 bytes (>> 4) to the low half never carries out
-// of the 14-bit start field.
+// Shared-memory matrix descriptor, K-major, no swizzle, as two 32-bit
+// halves: core matrices of 8 rows x 16 bytes; `lbo` = byte distance between
+// K-adjacent core matrices, `sbo` = byte distance between 8-row groups.
+// low = start address >> 4 | (lbo >> 4) << 16; high = sbo >> 4 | the tcgen05
+// descriptor version bit (bit 46 of the whole); base offset 0, no swizzle.
+// Shared-window addresses stay below 2^18, so adding a multiple of 16 bytes
+// (>> 4) to the low half never carries out of the 14-bit start field.
 __device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }

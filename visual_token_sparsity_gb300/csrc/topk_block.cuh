@@ -29,14 +29,6 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
 }
 
-// Histogram increment aggregated over the lanes of a warp that hit the same
-// bin (the leading digit of similar-magnitude floats falls into few bins, and
-// same-address shared atomics serialise).  bin < 0 adds nothing.
-__device__ __forceinline__ void hist_add(int* hist, int bin) {
-  const unsigned peers = __match_any_sync(__activemask(), bin);
-  if (bin >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-}
-
 // Block-wide exclusive scan of one value per thread (blockDim.x a multiple
 // of 32, at most 1024); unsigned types wrap modulo 2^32.
 template <typename T>
