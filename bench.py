@@ -392,6 +392,55 @@ def salience_measure(batch, steps, warmup, stream, tiny=False):
     return ss, ms, flops
 
 
+def prune_measure(batch, steps, stream, pk):
+    """Top-k prune + compaction (sv_prune_compact) and threshold prune
+    (sv_prune_threshold) of the SigLIP features on real salience: GB/s of the
+    algorithmic bytes (salience read, kept rows read and written, indices)."""
+    from visual_token_sparsity_gb300 import binding as sv, synth
+    ss = synth.siglip_salience(batch=batch)
+    q, k, feat = synth.draw_salience(ss, device="cuda")
+    B, N, C = ss.batch, ss.N, ss.C
+    sal = torch.empty(B, N, device="cuda")
+    ws = sv.workspace(max(sv.sv_salience_workspace_bytes(B, ss.H, N, ss.d), sv.sv_prune_workspace_bytes(B, N, N)))
+    sv.sv_salience_prefill(q, k, 1 / math.sqrt(ss.d), sal, ws)
+    del q, k
+    kept = torch.empty(B, ss.k, dtype=torch.int32, device="cuda")
+    fout = torch.empty(B, ss.k, C, dtype=torch.bfloat16, device="cuda")
+    tidx = torch.empty(B, N, dtype=torch.int32, device="cuda")
+    tcnt = torch.empty(B, dtype=torch.int32, device="cuda")
+    tout = torch.empty(B, N, C, dtype=torch.bfloat16, device="cuda")
+    thr = 1.0 / N     # the mean salience
+    calls = {"topk": lambda: sv.sv_prune_compact(sal, ss.k, feat, fout, kept, ws),
+             "threshold": lambda: sv.sv_prune_threshold(sal, thr, feat, tout, tidx, tcnt, ws)}
+    us = {}
+    for name, fn in calls.items():
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us[name] = e0.elapsed_time(e1) * 1e3 / steps
+    row = C * 2
+    kept_t = int(tcnt.sum().item())
+    b_topk = B * N * 4 + B * ss.k * (2 * row + 4)
+    b_thr = B * N * 4 + B * N * 4 + B * 4 + kept_t * 2 * row
+    out = {"workload": f"{ss.name}: {B} frames x {N} tokens, {C}-wide bf16 features",
+           "topk_us": us["topk"], "topk_keep": ss.keep, "topk_gbs": b_topk / (us["topk"] * 1e-6) / 1e9,
+           "threshold_us": us["threshold"], "threshold": "mean salience (1/N)",
+           "threshold_kept_fraction": kept_t / (B * N),
+           "threshold_gbs": b_thr / (us["threshold"] * 1e-6) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+           "peak_source": pk["source"],
+           "bytes": "salience read + kept feature rows read and written + indices"}
+    out["topk_frac"] = out["topk_gbs"] / pk["hbm_gbs"]
+    out["threshold_frac"] = out["threshold_gbs"] / pk["hbm_gbs"]
+    return out
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def oracle_sample_seconds(shape, units, seed=0):
@@ -591,6 +640,8 @@ def main():
                             "frac": tf / pk["bf16_tflops"], "peak_source": pk["source"],
                             "flop_count": "4*H*N^2*d per frame (both QK^T passes, d unpadded)"}
     if not a.no_salience and a.workload != "tiny":
+        line["prune"] = prune_measure(a.salience_batch, min(50, max(3, a.steps // 2)), stream, pk)
+        torch.cuda.empty_cache()
         cs = synth.clip_summary_salience(batch=a.salience_batch)
         us, nbytes = summary_salience_measure(cs, min(50, max(3, a.steps // 2)), stream)
         gbs = nbytes / (us * 1e-6) / 1e9
