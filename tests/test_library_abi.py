@@ -103,3 +103,32 @@ def test_workspace_sizes_are_monotone_in_tokens(so):
             prev = w
     assert lib.sv_retrieve_workspace_bytes(16, 32, 32, 128, 2880, 720) >= 256 + 16 * 32 * 2880 * 4
     assert lib.sv_salience_workspace_bytes(256, 16, 729, 72) >= 256 + 256 * 16 * 729 * 4
+
+
+def test_ctypes_structs_match_the_header_layout(tmp_path):
+    """The binding's ctypes mirrors of sv_kv_layer and sv_seq_batch have the
+    C compiler's size and field offsets (a probe compiled against sv.h)."""
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not available")
+    from visual_token_sparsity_gb300 import binding
+    probe = tmp_path / "layout.c"
+    fields = {"sv_kv_layer": [f for f, _ in binding.sv_kv_layer._fields_],
+              "sv_seq_batch": [f for f, _ in binding.sv_seq_batch._fields_]}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "sv.h"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'  printf("{st} size %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'  printf("{st} {f} %zu\\n", offsetof({st}, {f}));')
+    lines += ["  return 0;", "}"]
+    probe.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(probe), "-o", str(exe)],
+                   check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        st, f, v = line.split()
+        got[(st, f)] = int(v)
+    for st, cls in (("sv_kv_layer", binding.sv_kv_layer), ("sv_seq_batch", binding.sv_seq_batch)):
+        assert got[(st, "size")] == ctypes.sizeof(cls), st
+        for f, _ in cls._fields_:
+            assert got[(st, f)] == getattr(cls, f).offset, f"{st}.{f}"
