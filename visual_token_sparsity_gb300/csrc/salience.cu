@@ -10,7 +10,7 @@
 //
 // Design: persistent CTAs (one per SM), each walking over (frame, head)
 // units; 16 softmax warps, one MMA-issue warp and one TMA warp.  Per unit two
-// passes run back to back over 128-row tiles x 128-column chunks:
+// passes run back to back over 128-row tiles x 256-column chunks:
 //   pass 1  K_h resident in shared memory, 128-row tiles of Q_h streamed by
 //           TMA; S = Q_tile K_chunk^T (M=128, N<=256, K=d padded to 16) goes
 //           to one of two 256-column TMEM buffers; every softmax thread owns
