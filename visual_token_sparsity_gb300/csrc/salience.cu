@@ -81,7 +81,7 @@ struct SalGeom {
   int kc_load;  // 8-element K chunks that TMA loads (d / 8)
   int Np;       // N rounded up to 32 (columns that MMAs produce)
   int Rr;       // N rounded up to 128 (rows of a resident operand)
-  int nt;       // 128-row tiles = 128-column chunks
+  int nt;       // 128-row tiles = 128-row resident pieces
   size_t res_bytes, slot_bytes, smem_bytes;
 };
 
