@@ -659,6 +659,13 @@ def main():
         dist.destroy_process_group()
 
 
+def launches_per_layer(shape):
+    """Kernels one layer of the decode step launches (retrieval + attention)."""
+    from visual_token_sparsity_gb300 import binding as sv
+    return (sv.sv_retrieve_kernel_count(shape.n_vis) +
+            sv.sv_attn_kernel_count(shape.batch, shape.H, shape.Hkv, shape.k + shape.n_text))
+
+
 def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
     rb, ab = decode_bytes(shape)
     bytes_step = rb + ab
@@ -684,9 +691,9 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
     line.update({"value": value, "ms_per_step": ms, "decode_step_us": ms * 1e3,
             "attn_only_step_us": ms_attn * 1e3,
             "clocks": clk.summary(),
-            # per layer: fused retrieval (+ a separate top-k when the row exceeds
-            # the in-kernel limit) and the fused split-K attention
-            "gpu_launches": a.steps * shape.layers * ((1 if shape.n_vis <= 11264 else 2) + 1),
+            # per layer: retrieval (+ a separate top-k for long rows) and
+            # attention (+ a merge kernel for many splits), as the library reports
+            "gpu_launches": a.steps * shape.layers * launches_per_layer(shape),
             "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
                          "traffic": (measured_traffic(f"{dom[3]}:{shape.name}:b{shape.batch}:keep{shape.keep}")

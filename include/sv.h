@@ -127,6 +127,19 @@ size_t sv_retrieve_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, i
 size_t sv_attn_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n_tokens);
 size_t sv_evict_workspace_bytes(void);
 
+/*
+ * Kernels one call launches on its stream (pure host functions, for callers
+ * that budget launches, e.g. when building CUDA graphs):
+ *   sv_retrieve_kernel_count -- sv_retrieve_topk over rows of n_vis keys: 1
+ *     (the top-k runs inside the scoring kernel) or 2 (a separate top-k
+ *     kernel for long rows); 0 for n_vis <= 0.
+ *   sv_attn_kernel_count -- sv_sparse_decode_attn over n_tokens attended
+ *     tokens per (sequence, KV head): 1 (the split merge runs inside the
+ *     attention kernel) or 2 (a separate merge kernel); 0 for invalid sizes.
+ */
+int sv_retrieve_kernel_count(int n_vis);
+int sv_attn_kernel_count(int B, int H, int n_kv_heads, int n_tokens);
+
 /* ------------------------------------------------------------------------
  * Prefill salience -- velog.io summary §3.1 (salience table, "no summary
  * token" encoders such as SigLIP / QwenVL: the intra-visual attention a token

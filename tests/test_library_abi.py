@@ -132,3 +132,17 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
         assert got[(st, "size")] == ctypes.sizeof(cls), st
         for f, _ in cls._fields_:
             assert got[(st, f)] == getattr(cls, f).offset, f"{st}.{f}"
+
+
+def test_kernel_count_queries(so):
+    """Pure host queries: LLaVA-NeXT rows fuse the top-k and the split merge
+    (one kernel each); LongVILA's 50176-key rows need a separate top-k and its
+    12800-token splits a merge kernel."""
+    from visual_token_sparsity_gb300 import binding
+    lib = binding.load(so)
+    assert lib.sv_retrieve_kernel_count(2880) == 1
+    assert lib.sv_retrieve_kernel_count(50176) == 2
+    assert lib.sv_retrieve_kernel_count(0) == 0
+    assert lib.sv_attn_kernel_count(16, 32, 32, 1440 + 128) == 1
+    assert lib.sv_attn_kernel_count(8, 28, 4, 12544 + 256) == 2
+    assert lib.sv_attn_kernel_count(1, 28, 5, 100) == 0   # H not a multiple of n_kv_heads

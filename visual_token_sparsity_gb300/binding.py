@@ -48,6 +48,8 @@ _SIGS = {
     "sv_last_error": (ctypes.c_char_p, []),
     "sv_version": (ctypes.c_char_p, []),
     "sv_salience_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "sv_retrieve_kernel_count": (_I, [_I]),
+    "sv_attn_kernel_count": (_I, [_I, _I, _I, _I]),
     "sv_topk_workspace_bytes": (_SZ, [_I, _I, _I]),
     "sv_prune_workspace_bytes": (_SZ, [_I, _I, _I]),
     "sv_retrieve_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -202,6 +204,16 @@ def sv_attn_workspace_bytes(B, H, n_kv_heads, head_dim, n_tokens):
 
 def sv_evict_workspace_bytes():
     return load().sv_evict_workspace_bytes()
+
+
+def sv_retrieve_kernel_count(n_vis):
+    """Kernels one sv_retrieve_topk call launches (1: fused top-k, 2: separate top-k)."""
+    return load().sv_retrieve_kernel_count(int(n_vis))
+
+
+def sv_attn_kernel_count(B, H, n_kv_heads, n_tokens):
+    """Kernels one sv_sparse_decode_attn call launches (1: fused split merge, 2: merge kernel)."""
+    return load().sv_attn_kernel_count(int(B), int(H), int(n_kv_heads), int(n_tokens))
 
 
 # ------------------------------------------------------------------ calls

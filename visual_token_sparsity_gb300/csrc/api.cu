@@ -155,6 +155,16 @@ size_t sv_attn_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n
 
 size_t sv_evict_workspace_bytes(void) { return kStatusBytes; }
 
+int sv_retrieve_kernel_count(int n_vis) {
+  if (n_vis <= 0) return 0;
+  return sv::retrieve_fuses_topk(n_vis) ? 1 : 2;
+}
+
+int sv_attn_kernel_count(int B, int H, int n_kv_heads, int n_tokens) {
+  if (B <= 0 || H <= 0 || n_kv_heads <= 0 || H % n_kv_heads || n_tokens <= 0) return 0;
+  return sv::attn_kernel_count(B, n_kv_heads, H / n_kv_heads, n_tokens);
+}
+
 // ------------------------------------------------------------------ prefill
 
 sv_status sv_salience_prefill(const void* q, const void* k, int B, int H, int N, int d, float scale,

@@ -100,6 +100,10 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   return p;
 }
 
+int attn_kernel_count(int B, int Hkv, int G, int n_tokens) {
+  return attn_plan(B, Hkv, G, n_tokens).nsplit <= kFusedMergeMaxSplits ? 1 : 2;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kAttnWarps * 32, (G == 1 ? SV_ATTN_MIN_BLOCKS : 1))
 sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
