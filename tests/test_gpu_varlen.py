@@ -222,3 +222,15 @@ def test_calls_without_per_sequence_support_reject_the_arrays(lib):
     with pytest.raises(sv.SvError) as e:
         sv.sv_pack_kv(layer, seqs, vis, 16, dst, dseqs, ws)
     assert e.value.status == 2
+
+
+def test_binding_checks_the_per_sequence_arrays(lib):
+    from visual_token_sparsity_gb300 import binding as sv
+    bt = torch.zeros(3, 4, dtype=torch.int32, device=DEV)
+    nv = torch.tensor([40, 10, 0], dtype=torch.int32, device=DEV)
+    s = sv.SeqBatch(bt, 40, 8, nv, None, nv)
+    assert s.c.n_vis_seq == nv.data_ptr() and s.c.k_seq == nv.data_ptr() and not s.c.n_text_seq
+    with pytest.raises(ValueError):
+        sv.SeqBatch(bt, 40, 8, torch.zeros(2, dtype=torch.int32, device=DEV))
+    with pytest.raises(ValueError):
+        sv.SeqBatch(bt, 40, 8, None, torch.zeros(3, dtype=torch.int64, device=DEV))
