@@ -60,6 +60,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-packed", action="store_true", help="skip the pack-once KV comparison")
     p.add_argument("--no-varlen", action="store_true", help="skip the per-sequence-length decode step")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the LongVILA, tiny-case and round-loop objects of the default line")
     return p.parse_args()
 
 
@@ -244,6 +246,10 @@ class DecodeWorkload:
         for l in range(self.shape.layers):
             self.attend(l)
 
+    def retrieve_only_step(self):
+        for l in range(self.shape.layers):
+            self.retrieve(l)
+
     # pack-once KV: per layer a second paged layer holding, per (sequence, KV
     # head), the selected visual rows then the text rows contiguously
     def make_packed(self):
@@ -299,24 +305,23 @@ def replay_timed(g, steps, stream, barrier):
     return start.elapsed_time(end) / steps      # ms per step
 
 
-def per_call_times(wl, steps, stream):
-    """Average device time of each C-ABI call kind, timed with events on the stream."""
-    ev = lambda: torch.cuda.Event(enable_timing=True)
-    tr, ta = [], []
-    with torch.cuda.stream(stream):
-        for it in range(steps + 2):
-            for l in range(wl.shape.layers):
-                e0, e1, e2 = ev(), ev(), ev()
-                e0.record(stream)
-                wl.retrieve(l)
-                e1.record(stream)
-                wl.attend(l)
-                e2.record(stream)
-                if it >= 2:
-                    tr.append((e0, e1))
-                    ta.append((e1, e2))
-    torch.cuda.synchronize()
-    return (float(np.mean([a.elapsed_time(b) for a, b in tr])), float(np.mean([a.elapsed_time(b) for a, b in ta])))
+def decode_graph_times(wl, steps, warmup, stream, barrier, clocks=None):
+    """Device time per step (ms) of three CUDA graphs over all layers:
+    retrieval + attention, attention only and retrieval only.  Per-call
+    kernel times are the single-call graphs' step time / layers, so launch
+    gaps between graphs never count as kernel time."""
+    g_step = time_graph(wl.step, steps, max(3, warmup), stream)
+    g_attn = time_graph(wl.attn_only_step, steps, 3, stream)
+    g_ret = time_graph(wl.retrieve_only_step, steps, 3, stream)
+    if clocks is not None:
+        with clocks:
+            ms = replay_timed(g_step, steps, stream, barrier)
+    else:
+        ms = replay_timed(g_step, steps, stream, barrier)
+    ms_attn = replay_timed(g_attn, steps, stream, barrier)
+    ms_ret = replay_timed(g_ret, steps, stream, barrier)
+    del g_step, g_attn, g_ret
+    return ms, ms_attn, ms_ret
 
 
 def e2e_throughput(wl, steps, warmup, stream, bytes_step):
@@ -443,42 +448,130 @@ def prune_measure(batch, steps, stream, pk):
 
 # ---------------------------------------------------------------- CPU oracle
 
+def _one_unit(shape):
+    """(layer, sequence) unit shape of a decode workload: one layer, batch 1."""
+    from visual_token_sparsity_gb300 import synth
+    return synth.DecodeShape(shape.name, H=shape.H, Hkv=shape.Hkv, d=shape.d, n_vis=shape.n_vis,
+                             n_text=shape.n_text, layers=1, batch=1, keep=shape.keep, R=shape.R, seed=shape.seed)
+
+
+def _draw_unit(one, layer):
+    from visual_token_sparsity_gb300 import synth
+    bt = synth.random_block_table(1, one.max_blocks, one.num_blocks, seed=1, identity=True)
+    lay = synth.draw_decode_layer(one, layer, bt)
+    qr, qd = synth.draw_decode_queries(one, layer)
+    return (lay.k_logical.double().numpy(), lay.v_logical.double().numpy(), qr.double().numpy(),
+            qd.double().numpy())
+
+
+def _oracle_on_unit(one, unit):
+    """The oracle's retrieval + sparse attention on one drawn unit; returns seconds."""
+    import oracle
+    K, V, qr64, qd64 = unit
+    t0 = time.perf_counter()
+    idx, _ = oracle.retrieve_topk(qr64, K[:, :, :one.n_vis], one.k)
+    oracle.sparse_decode_attention(qd64, K, V, idx, one.n_vis, one.n_text)
+    return time.perf_counter() - t0
+
+
 def oracle_sample_seconds(shape, units, seed=0):
     """Run the fp64 oracle on `units` (layer, sequence) pairs of the decode
-    workload; returns (seconds, algorithmic bytes covered)."""
-    import oracle
-    from visual_token_sparsity_gb300 import synth
-    one = synth.DecodeShape(shape.name, H=shape.H, Hkv=shape.Hkv, d=shape.d, n_vis=shape.n_vis,
-                            n_text=shape.n_text, layers=1, batch=1, keep=shape.keep, R=shape.R, seed=shape.seed)
-    bt = synth.random_block_table(1, one.max_blocks, one.num_blocks, seed=1, identity=True)
-    total = 0.0
+    workload, starting at layer `seed`; returns (seconds, algorithmic bytes
+    covered).  Input drawing is not timed."""
+    one = _one_unit(shape)
     rb, ab = decode_bytes(one)
+    total = 0.0
     for u in range(units):
-        lay = synth.draw_decode_layer(one, u, bt)
-        qr, qd = synth.draw_decode_queries(one, u)
-        K = lay.k_logical.double().numpy()
-        V = lay.v_logical.double().numpy()
-        qr64, qd64 = qr.double().numpy(), qd.double().numpy()
-        t0 = time.perf_counter()
-        idx, _ = oracle.retrieve_topk(qr64, K[:, :, :one.n_vis], one.k)
-        oracle.sparse_decode_attention(qd64, K, V, idx, one.n_vis, one.n_text)
-        total += time.perf_counter() - t0
+        total += _oracle_on_unit(one, _draw_unit(one, seed + u))
     return total, units * (rb + ab)
 
 
-def cpu_baseline(shape, budget_s=10.0):
-    units, secs, nbytes = 0, 0.0, 0
-    while secs < budget_s and units < 1000:
-        t, b = oracle_sample_seconds(shape, 1, seed=units)
-        units += 1
-        secs += t
-        nbytes += b
-    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{units} (layer, sequence) units of the same workload, retrieval + sparse attention, "
-                      f"fp64 numpy, single thread"}
+def _oracle_worker(job):
+    """Process-pool task: draw one unit (its own layer) and run the oracle on
+    it `reps` times; returns (oracle seconds, bytes)."""
+    shape, layer, reps = job
+    one = _one_unit(shape)
+    unit = _draw_unit(one, layer)
+    rb, ab = decode_bytes(one)
+    secs = sum(_oracle_on_unit(one, unit) for _ in range(reps))
+    return secs, reps * (rb + ab)
 
 
-def rounds_main(a):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for l in out.splitlines():
+            if l.strip().lower().startswith("model name"):
+                return l.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+class OraclePool:
+    """Spawned worker processes (one per host core, single-threaded numpy)
+    that time the oracle on independent (layer, sequence) units.  Spawn, not
+    fork: the parent may already hold a CUDA context."""
+
+    def __init__(self, workers=None):
+        import multiprocessing as mp
+        self.n = workers or host_cores()
+        self.pool = mp.get_context("spawn").Pool(self.n)
+
+    def run(self, shape, reps, layer0=0):
+        """Every worker runs `reps` oracle passes on its own unit; the job's
+        time is the slowest worker's oracle time.  Returns (seconds, bytes)."""
+        res = self.pool.map(_oracle_worker, [(shape, layer0 + i, reps) for i in range(self.n)], chunksize=1)
+        return max(r[0] for r in res), sum(r[1] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(shape, budget_s=8.0, pool=None):
+    """The oracle as it stands on the host cores: single-threaded on one unit
+    repeated for ~budget_s, then on every core (one unit per worker, same
+    number of passes per worker)."""
+    one = _one_unit(shape)
+    rb, ab = decode_bytes(one)
+    unit = _draw_unit(one, 0)
+    reps, secs = 0, 0.0
+    while secs < budget_s and reps < 2000:
+        secs += _oracle_on_unit(one, unit)
+        reps += 1
+    single = (rb + ab) * reps / secs / 1e9
+    out = {"value": single, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu_model": cpu_model(),
+           "host_cores": host_cores(),
+           "sample": f"{reps} oracle passes over one (layer, sequence) unit of the same workload "
+                     f"(retrieval + sparse attention), fp64 numpy, single thread",
+           "single_thread_gbs": single}
+    own = pool is None
+    try:
+        pool = pool or OraclePool()
+        per_worker = max(1, int(reps * 0.75))
+        t, nb = pool.run(shape, per_worker, layer0=1)
+        out.update({"value": nb / t / 1e9, "cores": pool.n, "all_cores_gbs": nb / t / 1e9,
+                    "sample": f"all cores: {pool.n} single-threaded workers x {per_worker} oracle passes over "
+                              f"their own (layer, sequence) unit (retrieval + sparse attention, fp64 numpy), "
+                              f"time = the slowest worker's; single thread: {reps} passes over one unit"})
+    except Exception as e:   # the single-thread figure still stands
+        out["all_cores_error"] = str(e)[:200]
+    finally:
+        if own and pool is not None:
+            pool.close()
+    return out
+
+
+def rounds_measure(batch, steps, warmup, stream):
     """Latency of the 5-round loop on the tiny shapes: per round, evict the
     previous question/answer, append the 32-token question, retrieve the
     top-25% visual tokens with its 32 query rows, then 256 decode steps of
@@ -486,10 +579,7 @@ def rounds_main(a):
     cache state (visual tokens + 32-token prefix), so one CUDA graph of a
     round is replayed; inputs are seeded device buffers."""
     from visual_token_sparsity_gb300 import binding as sv, synth
-    torch.cuda.set_device(0)
-    import __graft_entry__
-    __graft_entry__.build()
-    s = synth.multiturn(batch=a.batch)
+    s = synth.multiturn(batch=batch)
     dev = torch.device("cuda", 0)
     bt = synth.random_block_table(s.batch, s.max_blocks, s.num_blocks, seed=synth.subseed(s.seed, 0, 98)).to(dev)
     lay = synth.draw_decode_layer(s, 0, bt, device=dev)
@@ -545,21 +635,75 @@ def rounds_main(a):
             pseqs.n_text += 1
             sv.sv_sparse_decode_attn(aq[t], scale, player, pseqs, None, 0, outs_p[t], None, ws_a)
 
+    graph = time_graph(one_round, steps, max(3, warmup), stream)
+    ms = replay_timed(graph, steps, stream, lambda: None)
+    graph_p = time_graph(one_round_packed, steps, max(3, warmup), stream)
+    ms_p = replay_timed(graph_p, steps, stream, lambda: None)
+    del graph, graph_p
+    return {"workload": "round loop: evict, append 32-token question, retrieve top-25% with 32 rows, "
+                        "256 x (append + sparse attention); 4 q / 2 KV heads, d 64, 576 visual + 32-token "
+                        f"prefix, batch {s.batch}",
+            "round_us": ms * 1e3, "per_decode_step_us": ms * 1e3 / 256,
+            "rounds_per_s": 1e3 / ms, "gpu_launches_per_round": 1 + 1 + 256 * 2,
+            "packed": {"round_us": ms_p * 1e3, "per_decode_step_us": ms_p * 1e3 / 256,
+                       "note": "same round with the selection packed once (sv_pack_kv) and dense "
+                               "attention over the packed pages"}}
+
+
+def rounds_main(a):
+    """The round loop as its own bench line (--workload rounds)."""
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
     stream = torch.cuda.Stream()
-    graph = time_graph(one_round, a.steps, max(3, a.warmup), stream)
-    ms = replay_timed(graph, a.steps, stream, lambda: None)
-    graph_p = time_graph(one_round_packed, a.steps, max(3, a.warmup), stream)
-    ms_p = replay_timed(graph_p, a.steps, stream, lambda: None)
-    print(json.dumps({"metric": "multi-turn round latency (tiny shapes)", "value": ms * 1e3, "unit": "us/round",
-                      "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "higher_is_better": False,
-                      "per_decode_step_us": ms * 1e3 / 256, "dtype": "bf16", "data": "synthetic",
-                      "gpu_launches": a.steps * (1 + 1 + 256 * 2),
-                      "packed": {"round_us": ms_p * 1e3, "per_decode_step_us": ms_p * 1e3 / 256,
-                                 "note": "same round with the selection packed once (sv_pack_kv) and dense "
-                                         "attention over the packed pages"},
-                      "config": {"workload": "round loop: evict, append 32-token question, retrieve top-25% "
-                                             "with 32 rows, 256 x (append + sparse attention); 4 q / 2 KV "
-                                             "heads, d 64, 576 visual + 32-token prefix", "batch": s.batch}}))
+    r = rounds_measure(a.batch, a.steps, a.warmup, stream)
+    print(json.dumps({"metric": "multi-turn round latency (tiny shapes)", "value": r["round_us"],
+                      "unit": "us/round", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+                      "higher_is_better": False, "per_decode_step_us": r["per_decode_step_us"], "dtype": "bf16",
+                      "data": "synthetic", "gpu_launches": a.steps * r["gpu_launches_per_round"],
+                      "packed": r["packed"], "config": {"workload": r["workload"], "batch": a.batch}}))
+
+
+def exp_bound(ss, ms, clocks):
+    """Exp-limited bound of the salience kernel: 2*H*N^2 exps per frame (one
+    per logit in each pass) at 32 ex2 results per clock per SM (measured on
+    GB300), at the SM clock sampled under load (else the maximum clock)."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = None
+    if clocks:
+        mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz")
+    mhz = mhz or 2070.0
+    exps = 2.0 * ss.H * ss.N * ss.N * ss.batch
+    bound_ms = exps / (32.0 * props.multi_processor_count * mhz * 1e6) * 1e3
+    return {"exp_bound_ms": bound_ms, "exp_frac": bound_ms / ms, "exp_bound_clock_mhz": mhz,
+            "exp_count": exps}
+
+
+def tiny_measure(dev, steps, stream):
+    """The tiny single-layer case: one decode step (retrieval with 1 query row,
+    keep 25%, then sparse attention) and the prefill salience + top-25% prune
+    and compaction on the 576-token encoder shape, each as a CUDA graph."""
+    from visual_token_sparsity_gb300 import binding as sv, synth
+    wl = DecodeWorkload(synth.tiny_decode(), dev)
+    ms, ms_attn, ms_ret = decode_graph_times(wl, steps, 3, stream, lambda: None)
+    ss = synth.tiny_salience()
+    q, k, feat = synth.draw_salience(ss, device=dev)
+    sal = torch.empty(ss.batch, ss.N, device=dev)
+    ws = sv.workspace(sv.sv_salience_workspace_bytes(ss.batch, ss.H, ss.N, ss.d), dev)
+    kept = torch.empty(ss.batch, ss.k, dtype=torch.int32, device=dev)
+    fout = torch.empty(ss.batch, ss.k, ss.C, dtype=torch.bfloat16, device=dev)
+    sal_fn = lambda: sv.sv_salience_prefill(q, k, 1 / math.sqrt(ss.d), sal, ws)
+    pre_fn = lambda: (sal_fn(), sv.sv_prune_compact(sal, ss.k, feat, fout, kept, ws))
+    g_sal = time_graph(sal_fn, steps, 3, stream)
+    ms_sal = replay_timed(g_sal, steps, stream, lambda: None)
+    g_pre = time_graph(pre_fn, steps, 3, stream)
+    ms_pre = replay_timed(g_pre, steps, stream, lambda: None)
+    del g_sal, g_pre, wl
+    return {"workload": "tiny: decode 4 q / 2 KV heads, d 64, 576 visual + 32 text, 1 query row, keep 25% "
+                        "(k=144), batch 1; prefill 576 tokens, 4 heads, d 64, keep 25%, 256-wide features",
+            "decode_step_us": ms * 1e3, "retrieve_us": ms_ret * 1e3, "attention_us": ms_attn * 1e3,
+            "salience_us": ms_sal * 1e3, "prefill_salience_prune_us": ms_pre * 1e3,
+            "note": "latency-bound (one small layer): microseconds only, graph replay"}
 
 
 # ---------------------------------------------------------------- main
@@ -590,21 +734,30 @@ def main():
     if a.impl == "reference":
         if rank != 0:
             return
-        for _ in range(a.warmup):
-            oracle_sample_seconds(shape, 1)
-        t, nb = 0.0, 0
-        for i in range(a.steps):
-            dt, b = oracle_sample_seconds(shape, 1, seed=i)
-            t += dt
-            nb += b
+        # the oracle on every host core: each step, every worker runs the
+        # oracle once on its own (layer, sequence) unit; the step's time is
+        # the slowest worker's
+        pool = OraclePool()
+        try:
+            for i in range(a.warmup):
+                pool.run(shape, 1, layer0=i * pool.n)
+            t, nb = 0.0, 0
+            for i in range(a.steps):
+                dt, b = pool.run(shape, 1, layer0=(a.warmup + i) * pool.n)
+                t += dt
+                nb += b
+        finally:
+            pool.close()
         v = nb / t / 1e9
         print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": a.gpus,
                           "steps": a.steps, "warmup": a.warmup, "ms_per_step": t / a.steps * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "config": config,
-                          "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                           "sample": "each step: one (layer, sequence) unit of the workload, "
-                                                     "retrieval + sparse attention, fp64 numpy, single thread"},
+                          "cpu_baseline": {"value": v, "unit": "GB/s", "cores": pool.n, "kind": "oracle",
+                                           "cpu_model": cpu_model(),
+                                           "sample": f"each step: {pool.n} single-threaded workers each run the "
+                                                     "oracle (retrieval + sparse attention, fp64 numpy) on their "
+                                                     "own (layer, sequence) unit of the workload"},
                           "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
 
@@ -629,21 +782,30 @@ def main():
             "config": config}
     if not a.no_decode:
         decode_measure(a, shape, dev, stream, barrier, world, pk, line)
+    extra_steps = min(50, max(3, a.steps // 2))
+    if not a.no_decode and not a.no_extra and a.workload == "llava":
+        # the other decode workloads as objects of the same line
+        lv = {}
+        for b in (8, 1):
+            lv[f"b{b}"] = decode_object(synth.longvila_decode(batch=b), dev, extra_steps, 3, stream, pk)
+        line["longvila"] = lv
+        line["tiny"] = tiny_measure(dev, extra_steps, stream)
+        line["rounds"] = rounds_measure(1, max(3, extra_steps // 4), 3, stream)
     if not a.no_salience:
         tiny = a.workload == "tiny"
-        ss, sms, flops = salience_measure(1 if tiny else a.salience_batch, min(50, max(3, a.steps // 2)), 3,
-                                          stream, tiny=tiny)
+        ss, sms, flops = salience_measure(1 if tiny else a.salience_batch, extra_steps, 3, stream, tiny=tiny)
         tf = flops / (sms * 1e-3) / 1e12
         line["salience"] = {"workload": f"{ss.name}: {ss.batch} frames x {ss.N} tokens, {ss.H} heads, d {ss.d}",
                             "ms": sms, "tokens_per_s": ss.batch * ss.N / (sms * 1e-3),
                             "tflops": tf, "bound": "tensor", "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": tf / pk["bf16_tflops"], "peak_source": pk["source"],
-                            "flop_count": "4*H*N^2*d per frame (both QK^T passes, d unpadded)"}
+                            "flop_count": "4*H*N^2*d per frame (both QK^T passes, d unpadded)",
+                            **exp_bound(ss, sms, line.get("clocks"))}
     if not a.no_salience and a.workload != "tiny":
-        line["prune"] = prune_measure(a.salience_batch, min(50, max(3, a.steps // 2)), stream, pk)
+        line["prune"] = prune_measure(a.salience_batch, extra_steps, stream, pk)
         torch.cuda.empty_cache()
         cs = synth.clip_summary_salience(batch=a.salience_batch)
-        us, nbytes = summary_salience_measure(cs, min(50, max(3, a.steps // 2)), stream)
+        us, nbytes = summary_salience_measure(cs, extra_steps, stream)
         gbs = nbytes / (us * 1e-6) / 1e9
         line["salience_summary"] = {
             "workload": f"{cs.name}: {cs.batch} frames x {cs.N} tokens, {cs.H} heads, d {cs.d}, 1 summary row",
@@ -666,41 +828,65 @@ def launches_per_layer(shape):
             sv.sv_attn_kernel_count(shape.batch, shape.H, shape.Hkv, shape.k + shape.n_text))
 
 
-def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
+def roofline_of(shape, ms_attn, ms_ret, pk, with_traffic=True):
+    """Roofline record of the dominant C call of a decode step.  The time per
+    launch is the single-call graph's step time / layers (graph replay over
+    all layers, inputs larger than L2); algorithmic bytes per launch follow
+    decode_bytes()."""
     rb, ab = decode_bytes(shape)
-    bytes_step = rb + ab
-    wl = DecodeWorkload(shape, dev)
-    g_step = time_graph(wl.step, a.steps, max(3, a.warmup), stream)
-    g_attn = time_graph(wl.attn_only_step, a.steps, 3, stream)
-
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        ms = replay_timed(g_step, a.steps, stream, barrier)
-    ms_attn = replay_timed(g_attn, a.steps, stream, barrier)
-    (ms, ms_attn), value = aggregate_replicas([ms, ms_attn], bytes_step, world,
-                                              torch_max_reducer(dev) if world > 1 else None)
-
-    t_ret, t_att = per_call_times(wl, min(20, max(3, a.steps // 4)), stream)
-    per_launch_ret = rb / (shape.layers)
-    per_launch_att = ab / (shape.layers)
+    t_ret, t_att = ms_ret / shape.layers, ms_attn / shape.layers
+    per_launch_ret, per_launch_att = rb / shape.layers, ab / shape.layers
     if t_att >= t_ret:
         dom = ("sv_sparse_decode_attn (split-K gather attention + combine)", per_launch_att, t_att, "attention")
     else:
         dom = ("sv_retrieve_topk (paged GEMV + radix top-k)", per_launch_ret, t_ret, "retrieve")
     achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+    return {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
+            "traffic": (measured_traffic(f"{dom[3]}:{shape.name}:b{shape.batch}:keep{shape.keep}")
+                        if with_traffic else None),
+            "algorithmic_bytes_per_launch": dom[1],
+            "timing": "graph replay of the call over all layers / layers",
+            "per_call_us": {"retrieve": t_ret * 1e3, "attention": t_att * 1e3},
+            "per_call_gbs": {"retrieve": per_launch_ret / (t_ret * 1e-3) / 1e9,
+                             "attention": per_launch_att / (t_att * 1e-3) / 1e9}}
 
+
+def decode_object(shape, dev, steps, warmup, stream, pk):
+    """Step figures of one more decode workload (its own cache, all layers)."""
+    rb, ab = decode_bytes(shape)
+    wl = DecodeWorkload(shape, dev)
+    ms, ms_attn, ms_ret = decode_graph_times(wl, steps, warmup, stream, lambda: None)
+    gbs = (rb + ab) / (ms * 1e-3) / 1e9
+    out = {"workload": f"{shape.name}: {shape.layers} layers, batch {shape.batch}, {shape.H} q / {shape.Hkv} KV "
+                       f"heads, d {shape.d}, {shape.n_vis} visual + {shape.n_text} text, keep {shape.keep} "
+                       f"(k={shape.k}), 1 query row",
+           "decode_step_us": ms * 1e3, "attn_only_step_us": ms_attn * 1e3, "retrieve_only_step_us": ms_ret * 1e3,
+           "gbs": gbs, "frac": gbs / pk["hbm_gbs"], "peak": pk["hbm_gbs"], "peak_source": pk["source"],
+           "attn_only_gbs": ab / (ms_attn * 1e-3) / 1e9,
+           "gpu_launches_per_step": shape.layers * launches_per_layer(shape),
+           "roofline": roofline_of(shape, ms_attn, ms_ret, pk)}
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
+def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
+    rb, ab = decode_bytes(shape)
+    bytes_step = rb + ab
+    wl = DecodeWorkload(shape, dev)
+    clk = ClockSampler(torch.cuda.current_device())
+    ms, ms_attn, ms_ret = decode_graph_times(wl, a.steps, a.warmup, stream, barrier, clocks=clk)
+    (ms, ms_attn, ms_ret), value = aggregate_replicas([ms, ms_attn, ms_ret], bytes_step, world,
+                                                      torch_max_reducer(dev) if world > 1 else None)
     line.update({"value": value, "ms_per_step": ms, "decode_step_us": ms * 1e3,
-            "attn_only_step_us": ms_attn * 1e3,
-            "clocks": clk.summary(),
-            # per layer: retrieval (+ a separate top-k for long rows) and
-            # attention (+ a merge kernel for many splits), as the library reports
-            "gpu_launches": a.steps * shape.layers * launches_per_layer(shape),
-            "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
-                         "traffic": (measured_traffic(f"{dom[3]}:{shape.name}:b{shape.batch}:keep{shape.keep}")
-                                     if world == 1 else None),
-                         "algorithmic_bytes_per_launch": dom[1],
-                         "per_call_us": {"retrieve": t_ret * 1e3, "attention": t_att * 1e3}},
-            "hbm_frac_step": (bytes_step / (ms * 1e-3) / 1e9) / pk["hbm_gbs"]})
+                 "attn_only_step_us": ms_attn * 1e3, "retrieve_only_step_us": ms_ret * 1e3,
+                 "clocks": clk.summary(),
+                 # per layer: retrieval (+ a separate top-k for long rows) and
+                 # attention (+ a merge kernel for many splits), as the library reports
+                 "gpu_launches": a.steps * shape.layers * launches_per_layer(shape),
+                 "roofline": roofline_of(shape, ms_attn, ms_ret, pk, with_traffic=world == 1),
+                 "hbm_frac_step": (bytes_step / (ms * 1e-3) / 1e9) / pk["hbm_gbs"]})
 
     if not a.no_e2e:
         e2e, h2d, d2h = e2e_throughput(wl, min(50, max(3, a.steps // 2)), 2, stream, bytes_step)
@@ -767,7 +953,7 @@ def decode_measure(a, shape, dev, stream, barrier, world, pk, line):
             "note": "retrieval + sparse attention per layer with per-sequence counts (sv_seq_batch n_vis_seq / "
                     "n_text_seq / k_seq); GB/s of the per-sequence algorithmic bytes"}
         del g_vl
-    del wl, g_step, g_attn
+    del wl
     torch.cuda.empty_cache()
 
 

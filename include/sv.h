@@ -268,9 +268,12 @@ sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer
  * nothing and calls no allocating routine.
  * Limit: batch * n_kv_heads * n_vis <= 2^21 (2,097,152 scores); larger calls
  * return SV_ERR_WORKSPACE without launching.
- * The first call on each device looks up the scratch array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.
+ * Every call looks up the scratch array's device address
+ * (cudaGetSymbolAddress) on the current device.  With lazy module loading
+ * (the CUDA default) the first call on each device loads this code and maps
+ * the 8 MiB array at that moment, which can fail with SV_ERR_CUDA (out of
+ * memory) when the caller's pool already holds nearly all device memory:
+ * make that first call at start-up, before any stream capture.
  * All calls share the one scratch array: calls that can overlap on the GPU
  * (different streams without ordering, or several host threads) race and
  * must not be issued.  The status word at the start of the scratch is

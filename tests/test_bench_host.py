@@ -45,3 +45,13 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"].startswith("llava-next-7b-decode")
+
+
+def test_cpu_baseline_reports_single_thread_and_all_cores():
+    """The oracle leg of the bench line: single-threaded and on every host
+    core (spawned workers), with the core count and CPU model recorded."""
+    d = bench.cpu_baseline(synth.tiny_decode(), budget_s=0.2)
+    assert d["kind"] == "oracle" and d["unit"] == "GB/s"
+    assert d["single_thread_gbs"] > 0 and d["all_cores_gbs"] > 0 and d["value"] == d["all_cores_gbs"]
+    assert d["cores"] == bench.host_cores() >= 1
+    assert isinstance(d["cpu_model"], str) and d["cpu_model"]

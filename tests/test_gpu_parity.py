@@ -84,11 +84,28 @@ def test_salience_zero_queries_exactly_uniform_and_prune_takes_first_k(lib):
     sv.sv_salience_prefill(q, k, 1 / math.sqrt(d), sal, ws)
     s = sal.cpu().numpy()
     assert np.abs(s - 1.0 / N).max() <= 1e-7
+    # every key sees the same logits (all 0) and the kernel sums them in the
+    # same order for every key, so each frame's row is exactly tied ...
+    assert (s == s[:, :1]).all(), "Q = 0 salience row is not exactly uniform"
+    # ... and a full tie goes to the lowest indices
     kept = torch.empty(B, 182, dtype=torch.int32, device=DEV)
-    # all scores tie up to fp32 rounding of 1/N: rows are exactly equal per frame
-    if (s == s[:, :1]).all():
-        sv.sv_prune_compact(sal, 182, None, None, kept, ws)
-        assert (kept.cpu().numpy() == np.arange(182)[None]).all()
+    sv.sv_prune_compact(sal, 182, None, None, kept, ws)
+    torch.cuda.synchronize()
+    assert (kept.cpu().numpy() == np.arange(182)[None]).all()
+
+
+@pytest.mark.parametrize("N,k", [(729, 182), (729, 364), (5000, 1250), (1, 1)])
+def test_prune_on_exactly_tied_rows_takes_first_k(lib, N, k):
+    from visual_token_sparsity_gb300 import binding as sv
+    B = 3
+    sal = torch.full((B, N), 1.0 / N, device=DEV)
+    sal[1] = -0.0      # signed zeros tie with each other
+    sal[1, ::2] = 0.0
+    ws = sv.workspace(sv.sv_prune_workspace_bytes(B, N, k))
+    kept = torch.empty(B, k, dtype=torch.int32, device=DEV)
+    sv.sv_prune_compact(sal, k, None, None, kept, ws)
+    torch.cuda.synchronize()
+    assert (kept.cpu().numpy() == np.arange(k)[None]).all()
 
 
 def test_salience_deterministic(lib):

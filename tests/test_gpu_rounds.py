@@ -127,17 +127,18 @@ def test_multiturn_rounds_match_oracle_and_do_not_leak(lib):
             n_used = shape.n_vis + nt
         K, V = oracle.append_tokens(K, V, n_used, qk.double().numpy(), qv.double().numpy())
         n_used += 32
-        idx_ref, sc_ref = oracle.retrieve_topk(rows.double().numpy(), K[:, :, :shape.n_vis], shape.k)
-        assert_selection(vis.cpu().numpy(), sc_ref, shape.k, f"round {r} retrieval")
-        same = np.array_equal(vis.cpu().numpy(), idx_ref)
+        _, sc_ref = oracle.retrieve_topk(rows.double().numpy(), K[:, :, :shape.n_vis], shape.k)
+        vis_np = vis.cpu().numpy()
+        assert_selection(vis_np, sc_ref, shape.k, f"round {r} retrieval")
+        # every decode step against the oracle over the GPU's own selection,
+        # so a legal swap inside the tie band cannot skip the comparison
         for t in range(256):
             K, V = oracle.append_tokens(K, V, n_used, ak[:, t:t + 1].double().numpy(),
                                         av[:, t:t + 1].double().numpy())
             n_used += 1
-            if same and (t % 16 == 0 or t == 255):
-                o_ref, _ = oracle.sparse_decode_attention(aq[:, t].double().numpy(), K, V, idx_ref,
-                                                          shape.n_vis, n_used - shape.n_vis)
-                assert_attention_close(outs[t], o_ref, f"round {r} step {t}")
+            o_ref, _ = oracle.sparse_decode_attention(aq[:, t].double().numpy(), K, V, vis_np,
+                                                      shape.n_vis, n_used - shape.n_vis)
+            assert_attention_close(outs[t], o_ref, f"round {r} step {t}")
         first_outs[r] = (vis.clone(), outs.clone())
         assert sv.sv_read_device_status(ws_a) == 0 and sv.sv_read_device_status(ws_e) == 0
     # no leakage: round 3 replayed on a cache that never saw rounds 0-2 gives the same bits

@@ -61,3 +61,30 @@ def test_noalloc_rejects_calls_beyond_the_fixed_scratch(lib):
     with pytest.raises(sv.SvError) as e:
         sv.sv_retrieve_topk_noalloc(q, layer, seqs, 10, idx)
     assert e.value.status == 4 and "scratch" in str(e.value)
+
+
+def test_noalloc_skips_a_bad_block_like_the_workspace_entry_point(lib):
+    """A block-table entry outside the pool: the workspace call reports it in
+    its status word; the workspace-free call (whose status word cannot be read
+    back) skips the same loads and gives the same indices and scores."""
+    from visual_token_sparsity_gb300 import binding as sv
+    shape = synth.tiny_decode(batch=2)
+    layer, seqs = _cache(shape)
+    bt = seqs.block_table.clone()
+    bt[1, 3] = shape.num_blocks            # one page of sequence 1 points past the pool
+    bad = sv.SeqBatch(bt, shape.n_vis, shape.n_text)
+    B, Hkv, k = shape.batch, shape.Hkv, shape.k
+    qr, _ = synth.draw_decode_queries(shape, 0, device=DEV)
+    ws = sv.workspace(sv.sv_retrieve_workspace_bytes(B, shape.H, Hkv, shape.d, shape.n_vis, k))
+    ref_idx = torch.empty(B, Hkv, k, dtype=torch.int32, device=DEV)
+    ref_sc = torch.empty(B, Hkv, shape.n_vis, device=DEV)
+    sv.sv_retrieve_topk(qr, layer, bad, k, ref_idx, ref_sc, ws)
+    assert sv.sv_read_device_status(ws) & sv.SV_DEV_BAD_BLOCK
+    idx = torch.full((B, Hkv, k), -1, dtype=torch.int32, device=DEV)
+    sc = torch.empty(B, Hkv, shape.n_vis, device=DEV)
+    sv.sv_retrieve_topk_noalloc(qr, layer, bad, k, idx, sc)
+    torch.cuda.synchronize()
+    assert torch.equal(sc, ref_sc)
+    assert torch.equal(idx, ref_idx)
+    # the skipped page's 16 tokens score 0 in both
+    assert (sc[1, :, 48:64] == 0).all()

@@ -9,6 +9,7 @@
 #include <cstring>
 
 #include "../../include/sv.h"
+#include "api_checks.h"
 #include "kernels.h"
 
 namespace sv {
@@ -56,26 +57,6 @@ sv_status check_ws(void* ws, size_t have, size_t need) {
   return SV_OK;
 }
 
-sv_status check_cache(const sv_kv_layer* L, const sv_seq_batch* S, bool need_v) {
-  if (!L || !S) return fail(SV_ERR_INVALID_ARG, "layer or batch descriptor is NULL");
-  if (!L->k_pool || (need_v && !L->v_pool) || !S->block_table)
-    return fail(SV_ERR_INVALID_ARG, "cache pool or block table pointer is NULL");
-  if (!aligned16(L->k_pool) || (need_v && !aligned16(L->v_pool)))
-    return fail(SV_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
-  if (L->head_dim != 64 && L->head_dim != 128)
-    return fail(SV_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", L->head_dim);
-  if (L->num_blocks <= 0 || L->n_kv_heads <= 0)
-    return fail(SV_ERR_INVALID_ARG, "num_blocks and n_kv_heads must be positive");
-  if ((long long)L->num_blocks * L->n_kv_heads * SV_BLOCK_TOKENS >= 0xffffffffLL)
-    return fail(SV_ERR_UNSUPPORTED, "pool has too many rows for 32-bit row ids");
-  if (S->batch < 0 || S->max_blocks <= 0 || S->n_vis < 0 || S->n_text < 0)
-    return fail(SV_ERR_INVALID_ARG, "negative batch or length");
-  if ((long long)S->n_vis + S->n_text > (long long)S->max_blocks * SV_BLOCK_TOKENS)
-    return fail(SV_ERR_INVALID_ARG, "n_vis + n_text = %d exceeds max_blocks * 16 = %d",
-                S->n_vis + S->n_text, S->max_blocks * SV_BLOCK_TOKENS);
-  return SV_OK;
-}
-
 // Per-sequence lengths of a batch view (all NULL: uniform lengths).
 sv::SeqLens lens_of(const sv_seq_batch* S) {
   sv::SeqLens l;
@@ -97,7 +78,42 @@ sv_status reject_lens(const sv_seq_batch* S, const char* call) {
 namespace sv {
 // Records `msg` as this thread's sv_last_error() text.
 void set_error_message(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
+sv_status check_cache(const sv_kv_layer* L, const sv_seq_batch* S, bool need_v) {
+  if (!L || !S) return fail(SV_ERR_INVALID_ARG, "layer or batch descriptor is NULL");
+  if (!L->k_pool || (need_v && !L->v_pool) || !S->block_table)
+    return fail(SV_ERR_INVALID_ARG, "cache pool or block table pointer is NULL");
+  if (!aligned16(L->k_pool) || (need_v && !aligned16(L->v_pool)))
+    return fail(SV_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
+  if (L->head_dim != 64 && L->head_dim != 128)
+    return fail(SV_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", L->head_dim);
+  if (L->num_blocks <= 0 || L->n_kv_heads <= 0)
+    return fail(SV_ERR_INVALID_ARG, "num_blocks and n_kv_heads must be positive");
+  if ((long long)L->num_blocks * L->n_kv_heads * SV_BLOCK_TOKENS >= 0xffffffffLL)
+    return fail(SV_ERR_UNSUPPORTED, "pool has too many rows for 32-bit row ids");
+  if (S->batch < 0 || S->max_blocks <= 0 || S->n_vis < 0 || S->n_text < 0)
+    return fail(SV_ERR_INVALID_ARG, "negative batch or length");
+  if ((long long)S->n_vis + S->n_text > (long long)S->max_blocks * SV_BLOCK_TOKENS)
+    return fail(SV_ERR_INVALID_ARG, "n_vis + n_text = %d exceeds max_blocks * 16 = %d",
+                S->n_vis + S->n_text, S->max_blocks * SV_BLOCK_TOKENS);
+  return SV_OK;
+}
+
+sv_status check_retrieve_args(const void* q, int R, int H, const sv_kv_layer* layer, const sv_seq_batch* seqs,
+                              int k, const int32_t* vis_idx) {
+  sv_status s = check_cache(layer, seqs, false);
+  if (s != SV_OK) return s;
+  if (!q || !vis_idx) return fail(SV_ERR_INVALID_ARG, "q and vis_idx must be non-NULL");
+  if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  const int Hkv = layer->n_kv_heads;
+  if (R <= 0 || H <= 0 || H % Hkv) return fail(SV_ERR_INVALID_ARG, "need R > 0 and H a multiple of n_kv_heads");
+  if (seqs->n_vis <= 0) return fail(SV_ERR_INVALID_ARG, "no visual tokens to retrieve from");
+  if (k < 1 || k > seqs->n_vis) return fail(SV_ERR_INVALID_ARG, "need 1 <= k <= n_vis (k = %d)", k);
+  return SV_OK;
+}
 }  // namespace sv
+
+using sv::check_cache;
 
 extern "C" {
 
@@ -274,14 +290,9 @@ sv_status sv_prune_compact(const float* salience, int B, int N, int k, const voi
 sv_status sv_retrieve_topk(const void* q, int R, int H, const sv_kv_layer* layer,
                            const sv_seq_batch* seqs, int k, int32_t* vis_idx, float* scores,
                            void* ws, size_t ws_bytes, void* stream) {
-  sv_status s = check_cache(layer, seqs, false);
+  sv_status s = sv::check_retrieve_args(q, R, H, layer, seqs, k, vis_idx);
   if (s != SV_OK) return s;
-  if (!q || !vis_idx) return fail(SV_ERR_INVALID_ARG, "q and vis_idx must be non-NULL");
-  if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q must be 16-byte aligned");
   const int Hkv = layer->n_kv_heads;
-  if (R <= 0 || H <= 0 || H % Hkv) return fail(SV_ERR_INVALID_ARG, "need R > 0 and H a multiple of n_kv_heads");
-  if (seqs->n_vis <= 0) return fail(SV_ERR_INVALID_ARG, "no visual tokens to retrieve from");
-  if (k < 1 || k > seqs->n_vis) return fail(SV_ERR_INVALID_ARG, "need 1 <= k <= n_vis (k = %d)", k);
   s = check_ws(ws, ws_bytes, sv_retrieve_workspace_bytes(seqs->batch, H, Hkv, layer->head_dim, seqs->n_vis, k));
   if (s != SV_OK) return s;
   if (seqs->batch == 0) return SV_OK;

@@ -12,32 +12,29 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its kNoAllocScratchBytes until the process exits.  Host code
 // must not pass the variable's name to a kernel (on the host it names a
-// host-side shadow, not device memory); the device address is looked up once
-// per device with cudaGetSymbolAddress, with that device current, on the first
-// call made on it.
+// host-side shadow, not device memory); every call looks up the device
+// address with cudaGetSymbolAddress on the current device.  The lookup is
+// cheap once the module is loaded, and it stays right if the context is
+// destroyed and recreated (the array may then sit at another address).  With
+// lazy module loading the first lookup on a device loads this module and
+// maps the array, which can fail when device memory is exhausted.
 #include <cuda_runtime.h>
 
 #include <cstdarg>
 #include <cstdio>
 
 #include "../../include/sv.h"
+#include "api_checks.h"
 #include "kernels.h"
-
-namespace sv {
-void set_error_message(const char* msg);
-}  // namespace sv
 
 namespace {
 
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kMaxScores = size_t(1) << 21;                  // fp32 scores: 8 MiB
 constexpr size_t kNoAllocScratchBytes = kStatusBytes + kMaxScores * sizeof(float);
-constexpr int kMaxDevices = 64;
 
 // [0, 256): device status word; [256, ...): scores [B][Hkv][n_vis].
 static __device__ __align__(256) unsigned char g_scratch[kNoAllocScratchBytes];
-
-void* g_scratch_addr[kMaxDevices] = {};
 
 sv_status noalloc_fail(sv_status s, const char* fmt, ...) {
   char buf[512];
@@ -49,20 +46,13 @@ sv_status noalloc_fail(sv_status s, const char* fmt, ...) {
   return s;
 }
 
-// Device address of g_scratch on the current device (set up on first use).
+// Device address of g_scratch in the current device's context.
 sv_status scratch_on_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return noalloc_fail(SV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(SV_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess || !p)
-      return noalloc_fail(SV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+  if (e != cudaSuccess || !p)
+    return noalloc_fail(SV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  *out = p;
   return SV_OK;
 }
 
@@ -71,21 +61,10 @@ sv_status scratch_on_current_device(void** out) {
 extern "C" sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const sv_kv_layer* layer,
                                               const sv_seq_batch* seqs, int k, int32_t* vis_idx,
                                               float* scores, void* stream) {
-  if (!layer || !seqs) return noalloc_fail(SV_ERR_INVALID_ARG, "layer or batch descriptor is NULL");
-  if (!q || !vis_idx || !layer->k_pool || !seqs->block_table)
-    return noalloc_fail(SV_ERR_INVALID_ARG, "q, vis_idx, k_pool and block_table must be non-NULL");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(layer->k_pool)) & 15u)
-    return noalloc_fail(SV_ERR_INVALID_ARG, "q and k_pool must be 16-byte aligned");
-  if (layer->head_dim != 64 && layer->head_dim != 128)
-    return noalloc_fail(SV_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", layer->head_dim);
+  // the checks of sv_retrieve_topk, so both entry points accept the same calls
+  sv_status s = sv::check_retrieve_args(q, R, H, layer, seqs, k, vis_idx);
+  if (s != SV_OK) return s;
   const int Hkv = layer->n_kv_heads;
-  if (layer->num_blocks <= 0 || Hkv <= 0) return noalloc_fail(SV_ERR_INVALID_ARG, "num_blocks and n_kv_heads must be positive");
-  if (R <= 0 || H <= 0 || H % Hkv) return noalloc_fail(SV_ERR_INVALID_ARG, "need R > 0 and H a multiple of n_kv_heads");
-  if (seqs->batch < 0 || seqs->max_blocks <= 0 || seqs->n_vis <= 0 || seqs->n_text < 0)
-    return noalloc_fail(SV_ERR_INVALID_ARG, "need batch >= 0, max_blocks > 0, n_vis > 0, n_text >= 0");
-  if ((long long)seqs->n_vis + seqs->n_text > (long long)seqs->max_blocks * SV_BLOCK_TOKENS)
-    return noalloc_fail(SV_ERR_INVALID_ARG, "n_vis + n_text exceeds max_blocks * 16");
-  if (k < 1 || k > seqs->n_vis) return noalloc_fail(SV_ERR_INVALID_ARG, "need 1 <= k <= n_vis (k = %d)", k);
   const size_t n_scores = (size_t)seqs->batch * Hkv * seqs->n_vis;
   if (n_scores > kMaxScores)
     return noalloc_fail(SV_ERR_WORKSPACE,
@@ -98,7 +77,7 @@ extern "C" sv_status sv_retrieve_topk_noalloc(const void* q, int R, int H, const
   lens.n_text = seqs->n_text_seq;
   lens.k = seqs->k_seq;
   void* base = nullptr;
-  sv_status s = scratch_on_current_device(&base);
+  s = scratch_on_current_device(&base);
   if (s != SV_OK) return s;
   int* status = static_cast<int*>(base);
   float* sc = scores ? scores : reinterpret_cast<float*>(static_cast<char*>(base) + kStatusBytes);
