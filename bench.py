@@ -60,6 +60,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-packed", action="store_true", help="skip the pack-once KV comparison")
     p.add_argument("--no-varlen", action="store_true", help="skip the per-sequence-length decode step")
+    p.add_argument("--salience-long-n", type=int, default=16384,
+                   help="tokens of the long-sequence salience object (0: skip it)")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the LongVILA, tiny-case and round-loop objects of the default line")
     return p.parse_args()
@@ -372,9 +374,9 @@ def summary_salience_measure(cs, steps, stream):
     return ms * 1e3, nbytes
 
 
-def salience_measure(batch, steps, warmup, stream, tiny=False):
+def salience_measure(batch, steps, warmup, stream, tiny=False, shape=None):
     from visual_token_sparsity_gb300 import binding as sv, synth
-    ss = synth.tiny_salience(batch=batch) if tiny else synth.siglip_salience(batch=batch)
+    ss = shape or (synth.tiny_salience(batch=batch) if tiny else synth.siglip_salience(batch=batch))
     q, k, _ = synth.draw_salience(ss, device="cuda")
     sal = torch.empty(ss.batch, ss.N, device="cuda")
     ws = sv.workspace(sv.sv_salience_workspace_bytes(ss.batch, ss.H, ss.N, ss.d))
@@ -801,6 +803,19 @@ def main():
                             "frac": tf / pk["bf16_tflops"], "peak_source": pk["source"],
                             "flop_count": "4*H*N^2*d per frame (both QK^T passes, d unpadded)",
                             **exp_bound(ss, sms, line.get("clocks"))}
+    if not a.no_salience and a.workload != "tiny" and a.salience_long_n > 0:
+        # long visual sequence: both operands streamed through 128 x 256 tiles
+        from visual_token_sparsity_gb300 import binding as sv
+        ls = synth.qwen2vl_salience(N=a.salience_long_n)
+        ls_, lms, lflops = salience_measure(1, max(3, extra_steps // 4), 3, stream, shape=ls)
+        ltf = lflops / (lms * 1e-3) / 1e12
+        line["salience_long"] = {
+            "workload": f"{ls.name}: {ls.batch} x {ls.N} tokens, {ls.H} heads, d {ls.d}",
+            "ms": lms, "tokens_per_s": ls.batch * ls.N / (lms * 1e-3), "tflops": ltf, "bound": "tensor",
+            "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": ltf / pk["bf16_tflops"],
+            "peak_source": pk["source"], "kernels_per_call": sv.sv_salience_kernel_count(ls.N, ls.d),
+            "flop_count": "4*H*N^2*d (both QK^T passes, d unpadded)", **exp_bound(ls, lms, line.get("clocks"))}
+        torch.cuda.empty_cache()
     if not a.no_salience and a.workload != "tiny":
         line["prune"] = prune_measure(a.salience_batch, extra_steps, stream, pk)
         torch.cuda.empty_cache()

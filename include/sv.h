@@ -138,6 +138,10 @@ size_t sv_evict_workspace_bytes(void);
  *     attention kernel) or 2 (a separate merge kernel); 0 for invalid sizes.
  */
 int sv_retrieve_kernel_count(int n_vis);
+/* sv_salience_prefill over N tokens of head dim d: 3 (salience kernel, its
+ * exact re-run of failed heads, head mean) or 4 for long sequences (row
+ * pass, its re-run, column pass, head mean); 0 for unsupported sizes. */
+int sv_salience_kernel_count(int N, int d);
 int sv_attn_kernel_count(int B, int H, int n_kv_heads, int n_tokens);
 
 /* ------------------------------------------------------------------------
@@ -152,11 +156,16 @@ int sv_attn_kernel_count(int B, int H, int n_kv_heads, int n_tokens);
  * q, k     : bf16 [B][H][N][d], contiguous.
  * scale    : logit scale (1/sqrt(d) for standard attention); must be > 0.
  * salience : out fp32 [B][N]; each row sums to 1.
- * Supported: d = 64 with N <= 1280, d = 72 with N <= 1024, d = 128 with
- * N <= 512 (one head's keys or queries stay resident in shared memory);
- * other shapes return SV_ERR_UNSUPPORTED.  Computed with tcgen05
- * tensor-core tiles (bf16 operands, fp32 accumulation) in two passes: row
- * log-sum-exp, then column accumulation.  Deterministic.
+ * Supported: d in {64, 72, 80, 128}, 1 <= N <= 2^24; other head dims return
+ * SV_ERR_UNSUPPORTED.  Computed with tcgen05 tensor-core tiles (bf16
+ * operands, fp32 accumulation) in two passes -- row log-sum-exp, then column
+ * accumulation with -lse folded into the MMA -- without forming the N x N
+ * matrix.  Short sequences (N <= 1024 at d 64 / 72, 768 at d 80, 512 at
+ * d 128) keep one head's keys or queries resident in shared memory; longer
+ * ones stream both operands through 128 x 256 tiles.  Row sums are taken without a running
+ * max; heads whose sums leave [2^-90, 2^100] are recomputed with one by a
+ * second, normally empty, launch.  Deterministic.
+ * ws_bytes >= sv_salience_workspace_bytes(B, H, N, d).
  */
 sv_status sv_salience_prefill(const void* q, const void* k, int B, int H, int N, int d,
                               float scale, float* salience, void* ws, size_t ws_bytes,

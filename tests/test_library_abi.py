@@ -68,7 +68,7 @@ def test_host_validation_rejects_before_launch(so):
     # salience: unsupported head dim, bad scale, too large N
     assert lib.sv_salience_prefill(_fake(), _fake(), 1, 1, 16, 96, 0.1, _fake(), _fake(), 1 << 20, s) == 2
     assert lib.sv_salience_prefill(_fake(), _fake(), 1, 1, 16, 64, -1.0, _fake(), _fake(), 1 << 20, s) == 1
-    assert lib.sv_salience_prefill(_fake(), _fake(), 1, 1, 4000, 128, 0.1, _fake(), _fake(), 1 << 30, s) == 2
+    assert lib.sv_salience_prefill(_fake(), _fake(), 1, 1, (1 << 24) + 1, 128, 0.1, _fake(), _fake(), 1 << 30, s) == 2
     # retrieval: k > n_vis, H not a multiple of Hkv, head dim 72 unsupported
     layer = binding.sv_kv_layer(_fake(), _fake(), 100, 2, 64)
     seqs = binding.sv_seq_batch(_fake(), 1, 10, 100, 10)
@@ -103,6 +103,23 @@ def test_workspace_sizes_are_monotone_in_tokens(so):
             prev = w
     assert lib.sv_retrieve_workspace_bytes(16, 32, 32, 128, 2880, 720) >= 256 + 16 * 32 * 2880 * 4
     assert lib.sv_salience_workspace_bytes(256, 16, 729, 72) >= 256 + 256 * 16 * 729 * 4
+    # the streamed schedule also keeps a 16-byte fold record per query
+    assert lib.sv_salience_workspace_bytes(1, 16, 16384, 80) >= 256 + 16 * 16384 * (4 + 16)
+
+
+def test_salience_schedule_switch_and_kernel_counts(so):
+    """Resident schedule up to 1024 tokens at d 64 / 72, 768 at d 80, 512 at
+    d 128 (3 kernels: salience, exact re-run, head mean); streamed beyond
+    (4 kernels: row pass, re-run, column pass, head mean)."""
+    from visual_token_sparsity_gb300 import binding
+    lib = binding.load(so)
+    for d, cap in ((64, 1024), (72, 1024), (80, 768), (128, 512)):
+        assert lib.sv_salience_kernel_count(1, d) == 3
+        assert lib.sv_salience_kernel_count(cap, d) == 3
+        assert lib.sv_salience_kernel_count(cap + 1, d) == 4
+        assert lib.sv_salience_kernel_count(50000, d) == 4
+    assert lib.sv_salience_kernel_count(100, 96) == 0
+    assert lib.sv_salience_kernel_count(0, 64) == 0
 
 
 def test_ctypes_structs_match_the_header_layout(tmp_path):

@@ -49,6 +49,7 @@ _SIGS = {
     "sv_version": (ctypes.c_char_p, []),
     "sv_salience_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "sv_retrieve_kernel_count": (_I, [_I]),
+    "sv_salience_kernel_count": (_I, [_I, _I]),
     "sv_attn_kernel_count": (_I, [_I, _I, _I, _I]),
     "sv_topk_workspace_bytes": (_SZ, [_I, _I, _I]),
     "sv_prune_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -204,6 +205,11 @@ def sv_attn_workspace_bytes(B, H, n_kv_heads, head_dim, n_tokens):
 
 def sv_evict_workspace_bytes():
     return load().sv_evict_workspace_bytes()
+
+
+def sv_salience_kernel_count(N, d):
+    """Kernels one sv_salience_prefill call launches (3, or 4 for long sequences)."""
+    return load().sv_salience_kernel_count(int(N), int(d))
 
 
 def sv_retrieve_kernel_count(n_vis):

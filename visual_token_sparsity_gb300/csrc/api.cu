@@ -13,7 +13,6 @@
 #include "kernels.h"
 
 namespace sv {
-size_t salience_smem_bytes(int N, int d);
 int topk_max_smem_keys();
 }  // namespace sv
 
@@ -136,8 +135,13 @@ const char* sv_version(void) { return "sv 0.1 sm_103a"; }
 // ------------------------------------------------------------------ sizes
 
 size_t sv_salience_workspace_bytes(int B, int H, int N, int d) {
-  if (B < 0 || H < 0 || N < 0) return kStatusBytes;
+  if (B < 0 || H < 0 || N <= 0 || !sv::salience_head_dim_supported(d)) return kStatusBytes;
   return kStatusBytes + round256(sv::salience_workspace_bytes(B, H, N, d));
+}
+
+int sv_salience_kernel_count(int N, int d) {
+  if (N <= 0 || !sv::salience_head_dim_supported(d)) return 0;
+  return sv::salience_kernel_count(N, d);
 }
 
 size_t sv_topk_workspace_bytes(int rows, int n, int k) {
@@ -188,11 +192,11 @@ sv_status sv_salience_prefill(const void* q, const void* k, int B, int H, int N,
   if (!q || !k || !salience) return fail(SV_ERR_INVALID_ARG, "q, k and salience must be non-NULL");
   if (B < 0 || H <= 0 || N <= 0) return fail(SV_ERR_INVALID_ARG, "need B >= 0, H > 0, N > 0");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale must be finite and > 0");
-  if (d != 64 && d != 72 && d != 128) return fail(SV_ERR_UNSUPPORTED, "salience head_dim %d (64, 72 or 128)", d);
+  if (!sv::salience_head_dim_supported(d))
+    return fail(SV_ERR_UNSUPPORTED, "salience head_dim %d (64, 72, 80 or 128)", d);
   if (!aligned16(q) || !aligned16(k)) return fail(SV_ERR_INVALID_ARG, "q and k must be 16-byte aligned");
-  if (sv::salience_smem_bytes(N, d) > kMaxSmemPerBlock)
-    return fail(SV_ERR_UNSUPPORTED, "N = %d too large for resident salience tiles at d = %d", N, d);
-  if ((long long)B * H > 0x7fffffffLL) return fail(SV_ERR_INVALID_ARG, "B * H too large");
+  if (N > (1 << 24)) return fail(SV_ERR_UNSUPPORTED, "N = %d > 2^24 tokens", N);
+  if ((long long)B * H * ((N + 127) / 128) > 0x7fffffffLL) return fail(SV_ERR_INVALID_ARG, "B * H * N too large");
   sv_status s = check_ws(ws, ws_bytes, sv_salience_workspace_bytes(B, H, N, d));
   if (s != SV_OK) return s;
   if (B == 0) return SV_OK;

@@ -122,6 +122,11 @@ cudaError_t launch_head_mean(const float* colsum, int B, int H, int N, float inv
 size_t summary_smem_bytes(int N, int d, int R);
 cudaError_t launch_summary_salience(const void* q, const void* k, int B, int H, int N, int d, int R,
                                     float scale, float* salience, float* colsum, cudaStream_t stream);
+bool salience_head_dim_supported(int d);
+// whether sv_salience_prefill streams both operands (long sequences) and how
+// many kernels one call launches
+bool salience_uses_long_schedule(int N, int d);
+int salience_kernel_count(int N, int d);
 size_t salience_workspace_bytes(int B, int H, int N, int d);
 cudaError_t launch_salience(const void* q, const void* k, int B, int H, int N, int d, float scale,
                             float* salience, void* ws, int* status, int num_sms,

@@ -167,6 +167,19 @@ __host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo) {
   return ((sbo >> 4) & 0x3FFFu) | (1u << 14);
 }
 
+// 128-byte swizzled K-major layout (what a TMA box with 128-byte swizzle
+// writes): rows of 128 bytes (64 bf16) in 8-row atoms of 1024 bytes, the
+// 16-byte units of row r XOR-permuted by r % 8.  `sbo` = 1024 (between 8-row
+// atoms); the leading offset is unused and encoded as 1; layout type 2 (bits
+// 61-63 of the whole).  A K-step of 16 inside the atom advances the start
+// address by 32 bytes.
+__device__ __forceinline__ uint32_t smem_desc_lo_sw128(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+__host__ __device__ constexpr uint32_t smem_desc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |

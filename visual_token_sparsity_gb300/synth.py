@@ -176,6 +176,14 @@ def clip_summary_salience(batch=256, keep=0.25):
                          C=1024, std=1.0 / math.sqrt(64.0), seed=6)
 
 
+def qwen2vl_salience(batch=1, N=16384, keep=0.25):
+    """Qwen2-VL vision tower (16 heads, d 80) over a long visual sequence:
+    N patch tokens of one high-resolution image or video clip; Q, K drawn
+    like the SigLIP frames (std 1/sqrt(d), 2% key outliers x4)."""
+    return SalienceShape("qwen2-vl-vision-salience", H=16, N=N, d=80, batch=batch, keep=keep, C=1280,
+                         std=1.0 / math.sqrt(80.0), seed=7)
+
+
 def longvila_decode(batch=1, layers=28):
     """Qwen2-7B attention (28 q heads, 4 KV heads, d 128), 256x196 visual + 256 text."""
     return DecodeShape("longvila-7b-decode", H=28, Hkv=4, d=128, n_vis=50176, n_text=256,
