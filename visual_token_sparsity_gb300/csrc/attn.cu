@@ -23,13 +23,13 @@
 #include "kernels.h"
 
 #ifndef SV_ATTN_TILE
-#define SV_ATTN_TILE 32        // tokens per warp step of the G <= 2 kernel
+#define SV_ATTN_TILE 8         // tokens per warp step of the G <= 2 kernel
 #endif
 #ifndef SV_ATTN_MMA_MIN_G
 #define SV_ATTN_MMA_MIN_G 3    // groups of at least this many heads use the tensor-core kernel
 #endif
 #ifndef SV_ATTN_MIN_BLOCKS
-#define SV_ATTN_MIN_BLOCKS 3   // resident CTAs per SM the G = 1 kernel is register-capped for
+#define SV_ATTN_MIN_BLOCKS 7   // resident CTAs per SM the G = 1 kernel is register-capped for
 #endif
 
 namespace sv {
@@ -46,7 +46,10 @@ struct AttnShape {
 };
 
 constexpr int kAttnWarps = 4;
-constexpr int kAttnTargetWarps = 4096;
+#ifndef SV_ATTN_TARGET_WARPS
+#define SV_ATTN_TARGET_WARPS 4096   // <= 152 SMs x 7 CTAs x 4 warps: one wave
+#endif
+constexpr int kAttnTargetWarps = SV_ATTN_TARGET_WARPS;
 constexpr int kAttnMaxSplits = 1024;
 constexpr int kFusedMergeMaxSplits = 32;   // above this a separate merge kernel runs
 constexpr uint32_t kNoRow = 0xffffffffu;
@@ -179,11 +182,8 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
     flag_status(status, kStatusBadBlock);
     return kNoRow;
   };
-  uint32_t next_rowid = lookup(load_pos(t_begin));
-  int pos_ahead = load_pos(t_begin + TILE);
-  for (int t0 = t_begin; t0 < t_end; t0 += TILE) {
-    const uint32_t rowid = next_rowid;
-    uint4 kd[NL], vd[NL];
+  // the TILE tokens' K and V rows for this lane (16 bytes each)
+  auto issue = [&](uint32_t rowid, uint4* kd, uint4* vd) {
 #pragma unroll
     for (int i = 0; i < NL; ++i) {
       const uint32_t r = __shfl_sync(0xffffffffu, rowid, i * TPI + lane / LPT);
@@ -195,10 +195,10 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
         vd[i] = make_uint4(0, 0, 0, 0);
       }
     }
+  };
+  // scores, online softmax and P.V of one tile
+  auto consume = [&](uint32_t rowid, const uint4* kd, const uint4* vd) {
     const bool mine_valid = __shfl_sync(0xffffffffu, rowid, my_tok) != kNoRow;
-    next_rowid = lookup(pos_ahead);
-    pos_ahead = load_pos(t0 + 2 * TILE);
-
     float p[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -246,6 +246,17 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
         for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(pj, v[e], o[hh][e]);
       }
     }
+  };
+
+  uint32_t next_rowid = lookup(load_pos(t_begin));
+  int pos_ahead = load_pos(t_begin + TILE);
+  for (int t0 = t_begin; t0 < t_end; t0 += TILE) {
+    const uint32_t rowid = next_rowid;
+    uint4 kd[NL], vd[NL];
+    issue(rowid, kd, vd);
+    next_rowid = lookup(pos_ahead);
+    pos_ahead = load_pos(t0 + 2 * TILE);
+    consume(rowid, kd, vd);
   }
 
   // fold the TPI lane groups and the per-lane softmax sums
