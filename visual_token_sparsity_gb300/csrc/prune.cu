@@ -1,40 +1,63 @@
 // Compaction of the kept prefill tokens (velog.io SparseVILA summary §2
 // table: pruned prefill tokens are physically deleted; §3.2 on dense packing
 // for coalesced reads).  out[b][t] = feat[b][idx[b][t]] for opaque rows of
-// row_bytes (a multiple of 16): a pure HBM copy with 16-byte vectors, one
-// warp per output row.
+// row_bytes (a multiple of 16): a pure HBM copy with 16-byte vectors.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk_block.cuh"
 
 namespace sv {
 
+// The output is one flat array of 16-byte vectors (rows x row_vecs); each
+// warp copies a contiguous stretch of kGatherU x 32 of them, so a lane issues
+// kGatherU independent loads before its first store whatever the row size,
+// and consecutive lanes touch consecutive bytes of the same source row.
 // counts (optional): frame b has counts[b] valid rows; later slots are skipped
+constexpr int kGatherU = 8;
 __global__ void __launch_bounds__(256)
-gather_rows_kernel(const uint4* __restrict__ feat, int N, int k, int64_t row_vecs,
-                   const int32_t* __restrict__ idx, uint4* __restrict__ out, long long rows,
+gather_rows_kernel(const uint4* __restrict__ feat, int N, int k, int row_vecs,
+                   const int32_t* __restrict__ idx, uint4* __restrict__ out, long long total,
                    const int32_t* __restrict__ counts, int* status) {
   const int lane = threadIdx.x & 31;
   const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long r = warp; r < rows; r += nwarps) {
-    const long long b = r / k;
-    if (counts && r - b * k >= __ldg(counts + b)) continue;
-    const int src = __ldg(idx + r);
-    uint4* dst = out + r * row_vecs;
-    if (src < 0 || src >= N) {
-      if (lane == 0) flag_status(status, kStatusBadIndex);
-      for (int64_t v = lane; v < row_vecs; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-      continue;
+  for (long long base = warp * (32 * kGatherU); base < total; base += nwarps * (32 * kGatherU)) {
+    // this lane's first vector: row r (slot rs of frame b), column c; the
+    // later ones follow 32 vectors apart
+    const long long i0 = base + lane;
+    long long r = i0 / row_vecs;
+    int c = (int)(i0 - r * row_vecs);
+    long long b = r / k;
+    int rs = (int)(r - b * k);
+    uint4 v[kGatherU];
+    long long dst[kGatherU];
+#pragma unroll
+    for (int u = 0; u < kGatherU; ++u) {
+      const long long i = i0 + u * 32;
+      dst[u] = -1;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < total && !(counts && rs >= __ldg(counts + b))) {
+        dst[u] = i;
+        const int src = __ldg(idx + r);
+        if (src < 0 || src >= N) {
+          if (c == 0) flag_status(status, kStatusBadIndex);   // the slot is written with zeros
+        } else {
+          v[u] = ld_stream16(feat + (b * N + src) * row_vecs + c);
+        }
+      }
+      c += 32;
+      while (c >= row_vecs) {
+        c -= row_vecs;
+        ++r;
+        if (++rs == k) {
+          rs = 0;
+          ++b;
+        }
+      }
     }
-    const uint4* s = feat + (b * N + src) * row_vecs;
-    int64_t v = lane;
-    for (; v + 96 < row_vecs; v += 128) {
-      const uint4 a0 = ld_stream16(s + v), a1 = ld_stream16(s + v + 32);
-      const uint4 a2 = ld_stream16(s + v + 64), a3 = ld_stream16(s + v + 96);
-      dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
-    }
-    for (; v < row_vecs; v += 32) dst[v] = ld_stream16(s + v);
+#pragma unroll
+    for (int u = 0; u < kGatherU; ++u)
+      if (dst[u] >= 0) out[dst[u]] = v[u];
   }
 }
 
@@ -42,13 +65,16 @@ cudaError_t launch_gather_rows(const void* feat, int B, int N, int k, int64_t ro
                                const int32_t* idx, void* out, int* status, cudaStream_t stream,
                                const int32_t* counts) {
   const long long rows = (long long)B * k;
-  if (rows == 0) return cudaSuccess;
+  const long long row_vecs = row_bytes / 16;
+  if (rows == 0 || row_vecs == 0) return cudaSuccess;
+  if (row_vecs > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const long long total = rows * row_vecs;
   const int threads = 256;
-  long long blocks = (rows + 7) / 8;
-  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  const long long per_block = (long long)threads * kGatherU;
+  long long blocks = (total + per_block - 1) / per_block;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;
   gather_rows_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      static_cast<const uint4*>(feat), N, k, row_bytes / 16, idx, static_cast<uint4*>(out), rows,
-      counts, status);
+      static_cast<const uint4*>(feat), N, k, (int)row_vecs, idx, static_cast<uint4*>(out), total, counts, status);
   return cudaGetLastError();
 }
 
