@@ -23,24 +23,27 @@
 #include "kernels.h"
 
 #ifndef SV_ATTN_TILE
-#define SV_ATTN_TILE 8         // tokens per warp step of the G <= 2 kernel
+#define SV_ATTN_TILE 8         // tokens per warp step of the G <= 2 kernel (large batches)
+#endif
+#ifndef SV_ATTN_SMALL_UNITS
+#define SV_ATTN_SMALL_UNITS 8  // at most this many (sequence, KV head) units: 32-token steps
 #endif
 #ifndef SV_ATTN_MMA_MIN_G
 #define SV_ATTN_MMA_MIN_G 3    // groups of at least this many heads use the tensor-core kernel
 #endif
 #ifndef SV_ATTN_MIN_BLOCKS
-#define SV_ATTN_MIN_BLOCKS 7   // resident CTAs per SM the G = 1 kernel is register-capped for
+#define SV_ATTN_MIN_BLOCKS 7   // resident CTAs per SM the G = 1, 8-token kernel is register-capped for
 #endif
 
 namespace sv {
 
 namespace {
 
-template <int D, int G>
+template <int D, int G, int TILE_ = SV_ATTN_TILE>
 struct AttnShape {
   static constexpr int LPT = D / 8;
   static constexpr int TPI = 32 / LPT;
-  static constexpr int TILE = G <= 2 ? SV_ATTN_TILE : (G <= 4 ? 16 : 8);
+  static constexpr int TILE = G <= 2 ? TILE_ : (G <= 4 ? 16 : 8);
   static constexpr int NL = TILE / TPI;
   static constexpr int DUP = LPT / NL;
 };
@@ -54,18 +57,24 @@ constexpr int kAttnMaxSplits = 1024;
 constexpr int kFusedMergeMaxSplits = 32;   // above this a separate merge kernel runs
 constexpr uint32_t kNoRow = 0xffffffffu;
 
-// tokens per warp step: 32 for the CUDA-core kernel (G <= 2), one 16-token
-// MMA sub-tile for the tensor-core kernel (attn_mma.cu, G >= 3)
+// tokens per warp step: one 16-token MMA sub-tile for the tensor-core kernel
+// (attn_mma.cu, G >= 3); for the CUDA-core kernel (G <= 2) 8-token steps at
+// 7 CTAs per SM when the batch fills the GPU, and 32-token steps for a few
+// (sequence, KV head) units, where fewer splits shorten the serial merge of
+// a latency-bound call
 bool attn_uses_mma(int G) { return G >= SV_ATTN_MMA_MIN_G; }
-int attn_tile(int G) { return attn_uses_mma(G) ? 16 : SV_ATTN_TILE; }
+int attn_tile(int G, long long units) {
+  if (attn_uses_mma(G)) return 16;
+  return units <= SV_ATTN_SMALL_UNITS ? 32 : SV_ATTN_TILE;
+}
 
 }  // namespace
 
 AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   AttnPlan p;
-  p.tile = attn_tile(G);
-  const int tiles = (n_tokens + p.tile - 1) / p.tile;
   const long long units = (long long)B * Hkv;
+  p.tile = attn_tile(G, units);
+  const int tiles = (n_tokens + p.tile - 1) / p.tile;
   long long tiles_total = units * (tiles > 0 ? tiles : 1);
   long long tpw = (tiles_total + kAttnTargetWarps - 1) / kAttnTargetWarps;
   if (tpw < 1) tpw = 1;
@@ -107,8 +116,8 @@ int attn_kernel_count(int B, int Hkv, int G, int n_tokens) {
   return attn_plan(B, Hkv, G, n_tokens).nsplit <= kFusedMergeMaxSplits ? 1 : 2;
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32, (G == 1 ? SV_ATTN_MIN_BLOCKS : 1))
+template <int D, int G, int TILE_>
+__global__ void __launch_bounds__(kAttnWarps * 32, (G == 1 ? (TILE_ <= 8 ? SV_ATTN_MIN_BLOCKS : 3) : 1))
 sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
                          const uint16_t* __restrict__ k_pool, const uint16_t* __restrict__ v_pool,
                          int num_blocks, int Hkv, const int32_t* __restrict__ block_table,
@@ -117,7 +126,7 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
                          float* __restrict__ part_ml, float* __restrict__ part_o, int* status,
                          int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse,
                          SeqLens lens) {
-  using S = AttnShape<D, G>;
+  using S = AttnShape<D, G, TILE_>;
   constexpr int LPT = S::LPT, TPI = S::TPI, TILE = S::TILE, NL = S::NL, DUP = S::DUP;
 
   const int lane = threadIdx.x & 31;
@@ -324,22 +333,28 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   if (lane == 0) split_done[bg] = 0;   // ready for the next call
 }
 
-template <int D, int G>
+template <int D, int G, int TILE>
 static void launch_split(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
   const long long warps = (long long)a.batch * a.Hkv * p.nsplit;
   const unsigned grid = (unsigned)((warps + kAttnWarps - 1) / kAttnWarps);
-  sparse_attn_split_kernel<D, G><<<grid, kAttnWarps * 32, 0, stream>>>(
+  sparse_attn_split_kernel<D, G, TILE><<<grid, kAttnWarps * 32, 0, stream>>>(
       static_cast<const uint16_t*>(a.q), a.H, static_cast<const uint16_t*>(a.k_pool),
       static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks,
       a.vis_idx, a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk,
       a.part_ml, a.part_o, a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse, a.lens);
 }
 
+template <int D, int G>
+static void launch_split_tile(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
+  if (p.tile == 32) launch_split<D, G, 32>(a, p, s);
+  else launch_split<D, G, SV_ATTN_TILE>(a, p, s);
+}
+
 template <int D>
 static bool dispatch_g(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
   switch (a.H / a.Hkv) {
-    case 1: launch_split<D, 1>(a, p, s); return true;
-    case 2: launch_split<D, 2>(a, p, s); return true;
+    case 1: launch_split_tile<D, 1>(a, p, s); return true;
+    case 2: launch_split_tile<D, 2>(a, p, s); return true;
     default: return false;
   }
 }
