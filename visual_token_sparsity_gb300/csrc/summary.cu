@@ -20,16 +20,23 @@ namespace sv {
 
 namespace {
 // 128 threads: more independent CTAs per SM overlap one CTA's load phase with
-// another's row reductions (measured faster than 256 or 512; batching more
-// than four token groups per lane costs occupancy, and staging the head's K
-// through one bulk copy into shared memory was slower)
+// another's row reductions (measured faster than 64, 256 or 512; staging the
+// head's K through bulk copies into shared memory, or splitting a head over
+// several CTAs, was slower)
 constexpr int kSumThreads = 128;
 constexpr int kSumWarps = kSumThreads / 32;
 
 size_t summary_smem(int N, int d, int R) { return ((size_t)R * d + (size_t)R * N + 2 * (size_t)R) * sizeof(float); }
 }  // namespace
 
-__global__ void __launch_bounds__(kSumThreads)
+// One summary row (CLIP): the query row stays in registers across the key
+// loop, six token groups per lane are in flight and the kernel is
+// register-capped for eight CTAs per SM; several rows (RADIO): four groups,
+// uncapped (measured on the 256-frame CLIP shape: one row, 6 groups, 8 CTAs
+// 59.0 us; 4 groups 60.7 us; 8 groups at 80 registers 69.7 us; the generic
+// loop over R rows 70.5 us)
+template <bool kOneRow>
+__global__ void __launch_bounds__(kSumThreads, kOneRow ? 8 : 1)
 summary_colsum_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, int N, int d, int R,
                       float sl2, float* __restrict__ colsum) {
   extern __shared__ float sm[];
@@ -51,26 +58,20 @@ summary_colsum_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
   while (lpt < cpr) lpt <<= 1;
   const int tpw = 32 / lpt;                        // tokens per warp step
   const int sub = lane % lpt, slot = lane / lpt;
-  // four token groups per iteration: their loads are all in flight before
-  // the first dot product needs one
-  constexpr int kU = 4;
+  // kSumU token groups per iteration, all loads in flight before the first
+  // dot product needs one; the raw 16-byte words stay packed (4 registers per
+  // group) until they are used
+  constexpr int kU = kOneRow ? 6 : 4;
   const int stride = kSumWarps * tpw;
   for (int j0 = warp * tpw; j0 < N; j0 += kU * stride) {
-    float kv[kU][8];
+    uint4 raw[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int j = j0 + u * stride + slot;
-      if (j < N && sub < cpr) {
-        const uint4 w4 = ld_stream16(kb + (size_t)j * d + sub * 8);
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) { kv[u][2 * c] = bf16_lo(w[c]); kv[u][2 * c + 1] = bf16_hi(w[c]); }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) kv[u][e] = 0.f;
-      }
+      raw[u] = (j < N && sub < cpr) ? ld_stream16(kb + (size_t)j * d + sub * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int r = 0; r < R; ++r) {
+    const int nr = kOneRow ? 1 : R;
+    for (int r = 0; r < nr; ++r) {
       float qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (sub < cpr) {
         const float* qr = qs + (size_t)r * d + sub * 8;
@@ -79,9 +80,13 @@ summary_colsum_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
+        const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(qv[e], kv[u][e], acc);
+        for (int c = 0; c < 4; ++c) {
+          acc = fmaf(qv[2 * c], bf16_lo(w[c]), acc);
+          acc = fmaf(qv[2 * c + 1], bf16_hi(w[c]), acc);
+        }
         for (int o = lpt >> 1; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         const int j = j0 + u * stride + slot;
         if (j < N && sub == 0) z[(size_t)r * N + j] = acc;
@@ -119,12 +124,16 @@ cudaError_t launch_summary_salience(const void* q, const void* k, int B, int H, 
   if (units == 0) return cudaSuccess;
   const size_t smem = summary_smem(N, d, R);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(summary_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(summary_colsum_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(summary_colsum_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  summary_colsum_kernel<<<(unsigned)units, kSumThreads, smem, stream>>>(
-      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), N, d, R, scale * kLog2e, colsum);
+  auto kern = R == 1 ? summary_colsum_kernel<true> : summary_colsum_kernel<false>;
+  kern<<<(unsigned)units, kSumThreads, smem, stream>>>(static_cast<const uint16_t*>(q),
+                                                        static_cast<const uint16_t*>(k), N, d, R, scale * kLog2e,
+                                                        colsum);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_head_mean(colsum, B, H, N, 1.0f / ((float)H * (float)R), salience, stream);
