@@ -10,9 +10,11 @@
 // Memory-bound.  A CTA scores a contiguous run of KV pages of one row; each
 // warp reads whole pages (16 tokens x d bf16, 2 or 4 KB, contiguous) with
 // 16-byte loads and folds the per-lane partial dot products with a butterfly
-// reduce-scatter (~d/8 shuffles per page).  One page in flight per warp at 32
-// registers (64 warps per SM) measured faster than a register-prefetched
-// second page at 104 registers.  The CTA that finishes a row last
+// reduce-scatter (~d/8 shuffles per page).  One page in flight per warp
+// measured faster than a register-prefetched second page at 104 registers;
+// capping the kernel at 48 registers (5 CTAs, 40 warps per SM; the fused
+// top-k spills a few words) measured 12 % faster than 64 registers (4 CTAs)
+// on LLaVA-NeXT rows and slower at 6 or 8 CTAs.  The CTA that finishes a row last
 // (a device-scope counter per row, no waiting) runs the exact block top-k on
 // that row's scores while other rows are still streaming, so no separate
 // selection kernel and no extra launch is needed when the row fits in shared
@@ -32,6 +34,9 @@ namespace sv {
 #ifndef SV_RET_WAVES
 #define SV_RET_WAVES 16        // target CTAs = SMs x this
 #endif
+#ifndef SV_RET_MINB
+#define SV_RET_MINB 5          // register cap: 5 resident CTAs (40 warps) per SM
+#endif
 
 namespace {
 constexpr int kRetrieveThreads = SV_RET_THREADS;
@@ -39,7 +44,7 @@ constexpr int kFuseMaxN = 11264;   // keys in dynamic shared memory (44 KB; stat
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(kRetrieveThreads)
+__global__ void __launch_bounds__(kRetrieveThreads, SV_RET_MINB)
 retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
                       const uint16_t* __restrict__ k_pool, int num_blocks, int Hkv,
                       const int32_t* __restrict__ block_table, int max_blocks, int n_vis,
