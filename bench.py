@@ -63,7 +63,7 @@ def parse():
     p.add_argument("--salience-long-n", type=int, default=16384,
                    help="tokens of the long-sequence salience object (0: skip it)")
     p.add_argument("--no-extra", action="store_true",
-                   help="skip the LongVILA, tiny-case and round-loop objects of the default line")
+                   help="skip the LongVILA, other LLaVA-NeXT, tiny-case and round-loop objects of the default line")
     return p.parse_args()
 
 
@@ -791,6 +791,13 @@ def main():
         for b in (8, 1):
             lv[f"b{b}"] = decode_object(synth.longvila_decode(batch=b), dev, extra_steps, 3, stream, pk)
         line["longvila"] = lv
+        # the other LLaVA-NeXT-7B cases: 25% keep at batch 16, batches 4 and 1
+        ln = {"b16_keep0.25": decode_object(synth.llava_next_decode(batch=16, keep=0.25), dev, extra_steps, 3,
+                                            stream, pk)}
+        for b in (4, 1):
+            ln[f"b{b}_keep0.5"] = decode_object(synth.llava_next_decode(batch=b, keep=0.5), dev, extra_steps, 3,
+                                                stream, pk)
+        line["llava_next"] = ln
         line["tiny"] = tiny_measure(dev, extra_steps, stream)
         line["rounds"] = rounds_measure(1, max(3, extra_steps // 4), 3, stream)
     if not a.no_salience:
