@@ -249,6 +249,12 @@ def test_retrieve_rows_equal_presummed_row(lib):
     (16, 1, 64, 300, 17, 2, 77, True),      # 16 heads per KV head (tensor-core tiles, no padding rows)
     (12, 1, 128, 500, 40, 1, 200, False),   # 12 heads per KV head
     (28, 4, 128, 50176, 256, 1, 12544, True),  # LongVILA shape, one sequence
+    # the CUDA-core kernel steps 32 tokens per warp for at most 8 (sequence,
+    # KV head) units and 8 tokens above: both sides of that switch, G 1 and 2
+    (8, 8, 128, 2880, 128, 1, 721, True),     # 8 units, G 1
+    (9, 9, 128, 2880, 128, 1, 719, False),    # 9 units, G 1
+    (8, 4, 64, 1000, 20, 2, 250, True),       # 8 units, G 2
+    (16, 8, 128, 2000, 60, 3, 333, True),     # 24 units, G 2
 ])
 def test_sparse_attention_matches_oracle(lib, H, Hkv, d, n_vis, n_text, B, k, sort):
     shape = synth.DecodeShape("t", H=H, Hkv=Hkv, d=d, n_vis=n_vis, n_text=n_text, layers=1, batch=B,
