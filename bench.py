@@ -402,7 +402,8 @@ def salience_measure(batch, steps, warmup, stream, tiny=False, shape=None):
 def prune_measure(batch, steps, stream, pk):
     """Top-k prune + compaction (sv_prune_compact) and threshold prune
     (sv_prune_threshold) of the SigLIP features on real salience: GB/s of the
-    algorithmic bytes (salience read, kept rows read and written, indices)."""
+    algorithmic bytes (salience read, kept rows read and written, indices),
+    device time per call from CUDA-graph replay."""
     from visual_token_sparsity_gb300 import binding as sv, synth
     ss = synth.siglip_salience(batch=batch)
     q, k, feat = synth.draw_salience(ss, device="cuda")
@@ -417,21 +418,16 @@ def prune_measure(batch, steps, stream, pk):
     tcnt = torch.empty(B, dtype=torch.int32, device="cuda")
     tout = torch.empty(B, N, C, dtype=torch.bfloat16, device="cuda")
     thr = 1.0 / N     # the mean salience
-    calls = {"topk": lambda: sv.sv_prune_compact(sal, ss.k, feat, fout, kept, ws),
-             "threshold": lambda: sv.sv_prune_threshold(sal, thr, feat, tout, tidx, tcnt, ws)}
+    # three feature copies, one per call of a graph: consecutive calls read
+    # rows of different copies (each call reads and writes more than L2 holds)
+    feats = [feat] + [feat.clone() for _ in range(2)]
+    calls = {"topk": lambda f: sv.sv_prune_compact(sal, ss.k, f, fout, kept, ws),
+             "threshold": lambda f: sv.sv_prune_threshold(sal, thr, f, tout, tidx, tcnt, ws)}
     us = {}
     for name, fn in calls.items():
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(steps):
-                fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        us[name] = e0.elapsed_time(e1) * 1e3 / steps
+        g = time_graph(lambda: [fn(f) for f in feats], steps, 3, stream)
+        us[name] = replay_timed(g, steps, stream, lambda: None) * 1e3 / len(feats)
+        del g
     row = C * 2
     kept_t = int(tcnt.sum().item())
     b_topk = B * N * 4 + B * ss.k * (2 * row + 4)

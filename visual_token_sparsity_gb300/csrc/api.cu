@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/sv.h"
@@ -13,6 +14,14 @@
 #include "kernels.h"
 
 namespace sv {
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("SV_PDL");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return on;
+}
 int topk_max_smem_keys();
 }  // namespace sv
 

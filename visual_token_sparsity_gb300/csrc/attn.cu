@@ -129,6 +129,7 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   using S = AttnShape<D, G, TILE_>;
   constexpr int LPT = S::LPT, TPI = S::TPI, TILE = S::TILE, NL = S::NL, DUP = S::DUP;
 
+  grid_dep_sync();
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kAttnWarps + (threadIdx.x >> 5);
   if (w >= (long long)batch * Hkv * nsplit) return;
@@ -334,28 +335,29 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
 }
 
 template <int D, int G, int TILE>
-static void launch_split(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
+static cudaError_t launch_split(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
   const long long warps = (long long)a.batch * a.Hkv * p.nsplit;
   const unsigned grid = (unsigned)((warps + kAttnWarps - 1) / kAttnWarps);
-  sparse_attn_split_kernel<D, G, TILE><<<grid, kAttnWarps * 32, 0, stream>>>(
-      static_cast<const uint16_t*>(a.q), a.H, static_cast<const uint16_t*>(a.k_pool),
-      static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks,
-      a.vis_idx, a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk,
-      a.part_ml, a.part_o, a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse, a.lens);
+  return launch_dependent(sparse_attn_split_kernel<D, G, TILE>, dim3(grid), dim3(kAttnWarps * 32), 0, stream,
+                          static_cast<const uint16_t*>(a.q), a.H, static_cast<const uint16_t*>(a.k_pool),
+                          static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks,
+                          a.vis_idx, a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk,
+                          a.part_ml, a.part_o, a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse,
+                          a.lens);
 }
 
 template <int D, int G>
-static void launch_split_tile(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
-  if (p.tile == 32) launch_split<D, G, 32>(a, p, s);
-  else launch_split<D, G, SV_ATTN_TILE>(a, p, s);
+static cudaError_t launch_split_tile(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
+  if (p.tile == 32) return launch_split<D, G, 32>(a, p, s);
+  return launch_split<D, G, SV_ATTN_TILE>(a, p, s);
 }
 
 template <int D>
-static bool dispatch_g(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
+static cudaError_t dispatch_g(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
   switch (a.H / a.Hkv) {
-    case 1: launch_split_tile<D, 1>(a, p, s); return true;
-    case 2: launch_split_tile<D, 2>(a, p, s); return true;
-    default: return false;
+    case 1: return launch_split_tile<D, 1>(a, p, s);
+    case 2: return launch_split_tile<D, 2>(a, p, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 
@@ -370,6 +372,7 @@ attn_merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ p
   extern __shared__ float wsh[];   // nsplit weights
   __shared__ float red[8];
   __shared__ float4 part[8][32];
+  grid_dep_sync();
   const int bh = blockIdx.x;
   const int b = bh / H, h = bh % H;
   const int g = h / G, hh = h % G;
@@ -443,13 +446,11 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   if (attn_uses_mma(G)) {
     e = launch_sparse_attn_mma(b, p, stream);
   } else {
-    const bool ok = a.D == 128 ? dispatch_g<128>(b, p, stream) : dispatch_g<64>(b, p, stream);
-    if (!ok) return cudaErrorInvalidValue;
-    e = cudaGetLastError();
+    e = a.D == 128 ? dispatch_g<128>(b, p, stream) : dispatch_g<64>(b, p, stream);
   }
   if (e != cudaSuccess || fused_merge) return e;
-  attn_merge_kernel<<<a.batch * a.H, 256, (size_t)p.nsplit * sizeof(float), stream>>>(
-      a.part_ml, a.part_o, a.H, a.Hkv, G, a.D, p.nsplit, static_cast<uint16_t*>(a.out), a.lse);
-  return cudaGetLastError();
+  return launch_dependent(attn_merge_kernel, dim3(a.batch * a.H), dim3(256), (size_t)p.nsplit * sizeof(float),
+                          stream, a.part_ml, a.part_o, a.H, a.Hkv, G, a.D, p.nsplit, static_cast<uint16_t*>(a.out),
+                          a.lse);
 }
 }  // namespace sv

@@ -76,6 +76,7 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
   constexpr int NT_O = D / 8;                        // output n-tiles (8 dims each)
   constexpr int TILE_BYTES = kSubTile * D * 2;       // one K or V sub-tile
   extern __shared__ __align__(128) uint8_t smem[];
+  grid_dep_sync();
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   uint8_t* my = smem + (size_t)wid * kMmaStages * 2 * TILE_BYTES;
@@ -371,11 +372,11 @@ cudaError_t launch_sparse_attn_mma(const AttnArgs& a, const AttnPlan& p, cudaStr
       a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk, a.part_ml, a.part_o,       \
       a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse, a.lens
   if (a.D == 128)
-    sparse_attn_mma_kernel<128><<<grid, kMmaWarps * 32, smem, stream>>>(SV_MMA_ARGS);
+    e = launch_dependent(sparse_attn_mma_kernel<128>, dim3(grid), dim3(kMmaWarps * 32), smem, stream, SV_MMA_ARGS);
   else
-    sparse_attn_mma_kernel<64><<<grid, kMmaWarps * 32, smem, stream>>>(SV_MMA_ARGS);
+    e = launch_dependent(sparse_attn_mma_kernel<64>, dim3(grid), dim3(kMmaWarps * 32), smem, stream, SV_MMA_ARGS);
 #undef SV_MMA_ARGS
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace sv

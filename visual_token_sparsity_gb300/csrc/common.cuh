@@ -17,6 +17,36 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void flag_status(int* status, int bits) { atomicOr(status, bits); }
 
+// Programmatic dependent launch.  A kernel launched by launch_dependent()
+// may become resident while the kernel before it in the stream drains; it
+// calls grid_dep_sync() first thing, which waits until that kernel has
+// completed and its memory operations are visible, and then lets its own
+// successor launch early.  Both are no-ops in an ordinary launch.
+__device__ __forceinline__ void grid_dep_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` with programmatic stream serialisation (overlapping its
+// launch and CTA rasterisation with the previous kernel's tail) unless the
+// environment sets SV_PDL=0.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Sequence b's visual, text and selected counts under `s`, whose capacities
 // are n_vis, n_text and k.  False (counts set to 0) when a count lies outside
 // [0, its capacity] or the selection exceeds the visual count: the caller

@@ -59,6 +59,7 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   __shared__ float qbar[D];
   __shared__ TopkShared ts;
   __shared__ int s_last;
+  grid_dep_sync();
   const int g = blockIdx.y;
   const int b = blockIdx.z;
   const int row = b * Hkv + g;
@@ -172,15 +173,13 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
   const uint16_t* qq = static_cast<const uint16_t*>(q);
   const uint16_t* kp = static_cast<const uint16_t*>(k_pool);
   int* done = fuse ? row_done : nullptr;
-  if (D == 128)
-    retrieve_score_kernel<128><<<grid, kRetrieveThreads, smem, stream>>>(
-        qq, R, H, G, kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
-        vis_idx, lens, n_text);
-  else
-    retrieve_score_kernel<64><<<grid, kRetrieveThreads, smem, stream>>>(
-        qq, R, H, G, kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
-        vis_idx, lens, n_text);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e =
+      D == 128 ? launch_dependent(retrieve_score_kernel<128>, grid, dim3(kRetrieveThreads), smem, stream, qq, R, H, G,
+                                  kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
+                                  vis_idx, lens, n_text)
+               : launch_dependent(retrieve_score_kernel<64>, grid, dim3(kRetrieveThreads), smem, stream, qq, R, H, G,
+                                  kp, num_blocks, Hkv, block_table, max_blocks, n_vis, per, scores, status, done, k,
+                                  vis_idx, lens, n_text);
   if (e != cudaSuccess || fuse) return e;
   if (topk_prefers_cluster(n_vis))
     return launch_topk_cluster(scores, rows, n_vis, k, vis_idx, stream, lens, Hkv);

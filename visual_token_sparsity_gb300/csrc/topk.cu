@@ -17,6 +17,7 @@ topk_rows_kernel(const float* __restrict__ scores, int n, int k, int32_t* __rest
                  int keys_in_smem, SeqLens lens, int rows_per_seq) {
   extern __shared__ uint32_t smem_keys[];
   __shared__ TopkShared ts;
+  grid_dep_sync();
   const int row = blockIdx.x;
   int nr = n, kr = k;
   if (lens.any()) row_lengths(lens, row, rows_per_seq, n, k, nr, kr);
@@ -43,9 +44,8 @@ cudaError_t launch_topk_rows(const float* scores, int rows, int n, int k, int32_
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  topk_rows_kernel<<<rows, threads, smem, stream>>>(scores, n, k, idx, in_smem ? 1 : 0, lens,
-                                                    rows_per_seq > 0 ? rows_per_seq : 1);
-  return cudaGetLastError();
+  return launch_dependent(topk_rows_kernel, dim3(rows), dim3(threads), smem, stream, scores, n, k, idx,
+                          in_smem ? 1 : 0, lens, rows_per_seq > 0 ? rows_per_seq : 1);
 }
 
 }  // namespace sv

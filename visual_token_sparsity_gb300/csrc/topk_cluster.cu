@@ -41,6 +41,7 @@ topk_cluster_kernel(const float* __restrict__ scores, int n_cap, int k_cap, int3
   __shared__ uint32_t cta_min, cta_max;
   __shared__ int sel_digit, sel_above, sel_count;
   __shared__ int cnt[2];          // this CTA's (greater, equal) counts
+  grid_dep_sync();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
@@ -239,9 +240,8 @@ cudaError_t launch_topk_cluster(const float* scores, int rows, int n, int k, int
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   dim3 grid(kTopkClusterCtas, rows);
-  topk_cluster_kernel<<<grid, kTopkClusterThreads, smem, stream>>>(scores, n, k, idx, lens,
-                                                                   rows_per_seq > 0 ? rows_per_seq : 1);
-  return cudaGetLastError();
+  return launch_dependent(topk_cluster_kernel, grid, dim3(kTopkClusterThreads), smem, stream, scores, n, k, idx,
+                          lens, rows_per_seq > 0 ? rows_per_seq : 1);
 }
 
 }  // namespace sv
