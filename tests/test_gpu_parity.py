@@ -29,7 +29,7 @@ def f64(t):
 
 @pytest.mark.parametrize("rows,n,k", [(1, 1, 1), (3, 15, 4), (2, 16, 16), (5, 17, 9), (4, 729, 182),
                                       (7, 2880, 720), (2, 50176, 12544), (1, 60000, 777),
-                                      (300, 576, 144)])
+                                      (300, 576, 144), (3, 20000, 1), (2, 40000, 40000), (33, 16385, 4097)])
 def test_topk_rows_bit_exact(lib, rows, n, k):
     from visual_token_sparsity_gb300 import binding as sv
     g = torch.Generator().manual_seed(rows * 1000 + n)
@@ -42,6 +42,23 @@ def test_topk_rows_bit_exact(lib, rows, n, k):
     sv.sv_topk_rows(x.to(DEV), k, idx, ws)
     ref = oracle.topk_ascending(x.double().numpy(), k)
     np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("n,k", [(20000, 7000), (50176, 12544)])
+def test_topk_long_rows_narrow_and_tied(lib, n, k):
+    """Long rows (the cluster path): values in a narrow positive range share
+    the high key bits (the first radix windows hold one bin), an all-equal
+    row takes the lowest indices, and a row of two values straddles k."""
+    from visual_token_sparsity_gb300 import binding as sv
+    g = torch.Generator().manual_seed(n)
+    narrow = 1000.0 + torch.randint(0, 300, (n,), generator=g).float() / 1024.0
+    equal = torch.full((n,), -3.5)
+    two = torch.where(torch.arange(n) % 3 == 0, torch.tensor(2.0), torch.tensor(1.0))
+    x = torch.stack([narrow, equal, two])
+    idx = torch.empty(3, k, dtype=torch.int32, device=DEV)
+    sv.sv_topk_rows(x.to(DEV), k, idx, sv.workspace(sv.sv_topk_workspace_bytes(3, n, k)))
+    np.testing.assert_array_equal(idx.cpu().numpy(), oracle.topk_ascending(x.double().numpy(), k))
+    assert (idx.cpu().numpy()[1] == np.arange(k)).all()
 
 
 def test_topk_all_equal_takes_lowest_indices(lib):
