@@ -842,7 +842,7 @@ def main():
 def launches_per_layer(shape):
     """Kernels one layer of the decode step launches (retrieval + attention)."""
     from visual_token_sparsity_gb300 import binding as sv
-    return (sv.sv_retrieve_kernel_count(shape.n_vis) +
+    return (sv.sv_retrieve_kernel_count(shape.batch, shape.Hkv, shape.n_vis) +
             sv.sv_attn_kernel_count(shape.batch, shape.H, shape.Hkv, shape.k + shape.n_text))
 
 

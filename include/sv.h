@@ -130,14 +130,15 @@ size_t sv_evict_workspace_bytes(void);
 /*
  * Kernels one call launches on its stream (pure host functions, for callers
  * that budget launches, e.g. when building CUDA graphs):
- *   sv_retrieve_kernel_count -- sv_retrieve_topk over rows of n_vis keys: 1
- *     (the top-k runs inside the scoring kernel) or 2 (a separate top-k
- *     kernel for long rows); 0 for n_vis <= 0.
+ *   sv_retrieve_kernel_count -- sv_retrieve_topk over batch * n_kv_heads
+ *     rows of n_vis keys: 1 (the top-k runs inside the scoring kernel: at
+ *     most 64 rows of at most 11264 keys) or 2 (a separate top-k kernel);
+ *     0 for n_vis <= 0.
  *   sv_attn_kernel_count -- sv_sparse_decode_attn over n_tokens attended
  *     tokens per (sequence, KV head): 1 (the split merge runs inside the
  *     attention kernel) or 2 (a separate merge kernel); 0 for invalid sizes.
  */
-int sv_retrieve_kernel_count(int n_vis);
+int sv_retrieve_kernel_count(int batch, int n_kv_heads, int n_vis);
 /* sv_salience_prefill over N tokens of head dim d: 3 (salience kernel, its
  * exact re-run of failed heads, head mean) or 4 for long sequences (row
  * pass, its re-run, column pass, head mean); 0 for unsupported sizes. */

@@ -157,9 +157,10 @@ def test_kernel_count_queries(so):
     12800-token splits a merge kernel."""
     from visual_token_sparsity_gb300 import binding
     lib = binding.load(so)
-    assert lib.sv_retrieve_kernel_count(2880) == 1
-    assert lib.sv_retrieve_kernel_count(50176) == 2
-    assert lib.sv_retrieve_kernel_count(0) == 0
+    assert lib.sv_retrieve_kernel_count(1, 32, 2880) == 1     # a few rows: top-k fused
+    assert lib.sv_retrieve_kernel_count(16, 32, 2880) == 2    # many rows: separate top-k
+    assert lib.sv_retrieve_kernel_count(1, 4, 50176) == 2     # long rows
+    assert lib.sv_retrieve_kernel_count(1, 4, 0) == 0
     assert lib.sv_attn_kernel_count(16, 32, 32, 1440 + 128) == 1
     assert lib.sv_attn_kernel_count(8, 28, 4, 12544 + 256) == 2
     assert lib.sv_attn_kernel_count(1, 28, 5, 100) == 0   # H not a multiple of n_kv_heads

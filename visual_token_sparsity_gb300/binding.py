@@ -48,7 +48,7 @@ _SIGS = {
     "sv_last_error": (ctypes.c_char_p, []),
     "sv_version": (ctypes.c_char_p, []),
     "sv_salience_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
-    "sv_retrieve_kernel_count": (_I, [_I]),
+    "sv_retrieve_kernel_count": (_I, [_I, _I, _I]),
     "sv_salience_kernel_count": (_I, [_I, _I]),
     "sv_attn_kernel_count": (_I, [_I, _I, _I, _I]),
     "sv_topk_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -212,9 +212,9 @@ def sv_salience_kernel_count(N, d):
     return load().sv_salience_kernel_count(int(N), int(d))
 
 
-def sv_retrieve_kernel_count(n_vis):
+def sv_retrieve_kernel_count(batch, n_kv_heads, n_vis):
     """Kernels one sv_retrieve_topk call launches (1: fused top-k, 2: separate top-k)."""
-    return load().sv_retrieve_kernel_count(int(n_vis))
+    return load().sv_retrieve_kernel_count(int(batch), int(n_kv_heads), int(n_vis))
 
 
 def sv_attn_kernel_count(B, H, n_kv_heads, n_tokens):

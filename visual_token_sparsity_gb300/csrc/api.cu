@@ -184,9 +184,9 @@ size_t sv_attn_workspace_bytes(int B, int H, int n_kv_heads, int head_dim, int n
 
 size_t sv_evict_workspace_bytes(void) { return kStatusBytes; }
 
-int sv_retrieve_kernel_count(int n_vis) {
+int sv_retrieve_kernel_count(int batch, int n_kv_heads, int n_vis) {
   if (n_vis <= 0) return 0;
-  return sv::retrieve_fuses_topk(n_vis) ? 1 : 2;
+  return sv::retrieve_fuses_topk(batch * n_kv_heads, n_vis) ? 1 : 2;
 }
 
 int sv_attn_kernel_count(int B, int H, int n_kv_heads, int n_tokens) {

@@ -70,7 +70,7 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens);
 // kernels one attention call launches: 1 (split merge fused), or 2 (merge kernel)
 int attn_kernel_count(int B, int Hkv, int G, int n_tokens);
 // whether the retrieval top-k runs inside the scoring kernel (rows of n_vis keys)
-bool retrieve_fuses_topk(int n_vis);
+bool retrieve_fuses_topk(int rows, int n_vis);
 
 struct AttnArgs {
   const void* q;

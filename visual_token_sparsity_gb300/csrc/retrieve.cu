@@ -14,11 +14,12 @@
 // measured faster than a register-prefetched second page at 104 registers;
 // capping the kernel at 48 registers (5 CTAs, 40 warps per SM; the fused
 // top-k spills a few words) measured 12 % faster than 64 registers (4 CTAs)
-// on LLaVA-NeXT rows and slower at 6 or 8 CTAs.  The CTA that finishes a row last
-// (a device-scope counter per row, no waiting) runs the exact block top-k on
-// that row's scores while other rows are still streaming, so no separate
-// selection kernel and no extra launch is needed when the row fits in shared
-// memory.
+// on LLaVA-NeXT rows and slower at 6 or 8 CTAs.  For calls with a few rows
+// the CTA that finishes a row last (a device-scope counter per row, no
+// waiting) runs the exact block top-k on that row's scores while other rows
+// are still streaming, so no separate selection kernel is launched; calls
+// with many rows, or rows too long for shared memory, select in a separate
+// top-k kernel.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk_block.cuh"
@@ -41,6 +42,12 @@ namespace sv {
 namespace {
 constexpr int kRetrieveThreads = SV_RET_THREADS;
 constexpr int kFuseMaxN = 11264;   // keys in dynamic shared memory (44 KB; static + dynamic < 48 KB)
+// The fused selection pays off for a few rows, where it overlaps the
+// streaming of the others; with many rows the last wave's selections form a
+// tail, and a separate top-k launch (overlapped with the scoring kernel's
+// drain) measured faster: LLaVA-NeXT rows, 128 and 512 rows 2.3-2.7 us per
+// call faster separate, 32 rows 1.4 us faster fused.
+constexpr int kFuseMaxRows = 64;
 }  // namespace
 
 template <int D>
@@ -152,7 +159,7 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   if (tid == 0) row_done[row] = 0;   // ready for the next call
 }
 
-bool retrieve_fuses_topk(int n_vis) { return n_vis <= kFuseMaxN; }
+bool retrieve_fuses_topk(int rows, int n_vis) { return rows <= kFuseMaxRows && n_vis <= kFuseMaxN; }
 
 cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_pool, int num_blocks,
                             int Hkv, int D, const int32_t* block_table, int max_blocks, int n_vis,
@@ -167,7 +174,7 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
   if (per < 8) per = 8;
   if (per > n_vblocks) per = n_vblocks;
   const int grid_x = (n_vblocks + per - 1) / per;
-  const bool fuse = row_done != nullptr && retrieve_fuses_topk(n_vis);
+  const bool fuse = row_done != nullptr && retrieve_fuses_topk(rows, n_vis);
   const size_t smem = fuse ? (size_t)n_vis * sizeof(uint32_t) : 0;
   dim3 grid(grid_x, Hkv, batch);
   const uint16_t* qq = static_cast<const uint16_t*>(q);
