@@ -27,6 +27,8 @@ def f64(t):
     (2, 1, 1, 128, 1, 1.0),          # a single token
     (1, 3, 2000, 128, 16, 1.0),      # largest R
     (1, 2, 33, 256, 2, 1.0),         # largest head dim
+    (2, 9, 150, 64, 1, 1.0),         # an odd head count
+    (1, 20, 300, 64, 2, 1.0),        # 20 heads
 ])
 def test_summary_salience_matches_oracle(lib, B, H, N, d, R, std):
     from visual_token_sparsity_gb300 import binding as sv
@@ -40,6 +42,19 @@ def test_summary_salience_matches_oracle(lib, B, H, N, d, R, std):
     torch.cuda.synchronize()
     assert sv.sv_read_device_status(ws) == 0
     assert_salience_close(sal.cpu().numpy(), oracle.summary_salience(f64(q), f64(k), R))
+
+
+def test_summary_salience_deterministic(lib):
+    from visual_token_sparsity_gb300 import binding as sv
+    B, H, N, d = 4, 16, 577, 64
+    q = synth.normal_bf16((B, H, N, d), 21, std=1 / 8).to(DEV)
+    k = synth.normal_bf16((B, H, N, d), 22, std=1 / 8).to(DEV)
+    ws = sv.workspace(sv.sv_salience_summary_workspace_bytes(B, H, N, d, 1))
+    a = torch.empty(B, N, device=DEV)
+    b = torch.empty(B, N, device=DEV)
+    sv.sv_salience_summary(q, k, 1, 0.125, a, ws)
+    sv.sv_salience_summary(q, k, 1, 0.125, b, ws)
+    assert torch.equal(a, b)
 
 
 def test_summary_salience_with_all_rows_equals_full_salience(lib):

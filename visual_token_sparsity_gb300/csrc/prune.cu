@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ feat, int N, int k, int row_vecs,
                    const int32_t* __restrict__ idx, uint4* __restrict__ out, long long total,
                    const int32_t* __restrict__ counts, int* status) {
+  grid_dep_sync();
   const int lane = threadIdx.x & 31;
   const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -73,9 +74,9 @@ cudaError_t launch_gather_rows(const void* feat, int B, int N, int k, int64_t ro
   const long long per_block = (long long)threads * kGatherU;
   long long blocks = (total + per_block - 1) / per_block;
   if (blocks > 65535LL * 16) blocks = 65535LL * 16;
-  gather_rows_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      static_cast<const uint4*>(feat), N, k, (int)row_vecs, idx, static_cast<uint4*>(out), total, counts, status);
-  return cudaGetLastError();
+  return launch_dependent(gather_rows_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                          static_cast<const uint4*>(feat), N, k, (int)row_vecs, idx, static_cast<uint4*>(out), total,
+                          counts, status);
 }
 
 // Threshold prune (xllm-io review §五 query_agnostic_pruning: keep the tokens
@@ -87,6 +88,7 @@ threshold_select_kernel(const float* __restrict__ sal, int N, float threshold, i
                         int32_t* __restrict__ count) {
   __shared__ int scan_tmp[33];
   __shared__ int s_total;
+  grid_dep_sync();
   const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   const float* s = sal + (size_t)b * N;
   int32_t* dst = idx + (size_t)b * N;
@@ -108,8 +110,7 @@ threshold_select_kernel(const float* __restrict__ sal, int N, float threshold, i
 cudaError_t launch_threshold_select(const float* sal, int B, int N, float threshold, int32_t* idx, int32_t* count,
                                     cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  threshold_select_kernel<<<B, 512, 0, stream>>>(sal, N, threshold, idx, count);
-  return cudaGetLastError();
+  return launch_dependent(threshold_select_kernel, dim3(B), dim3(512), 0, stream, sal, N, threshold, idx, count);
 }
 
 }  // namespace sv

@@ -832,6 +832,7 @@ cudaError_t run_salience(const void* q, const void* k, int B, int H, int N, int 
 // for the full salience, 1 / (H R) for the summary-row salience).
 __global__ void salience_head_mean_kernel(const float* __restrict__ colsum, int B, int H, int N,
                                           float inv, float* __restrict__ out) {
+  grid_dep_sync();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)B * N) return;
   const long long b = i / N, j = i % N;
@@ -845,8 +846,8 @@ cudaError_t launch_head_mean(const float* colsum, int B, int H, int N, float inv
                              cudaStream_t stream) {
   const long long total = (long long)B * N;
   if (total == 0) return cudaSuccess;
-  salience_head_mean_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(colsum, B, H, N, inv, out);
-  return cudaGetLastError();
+  return launch_dependent(salience_head_mean_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, stream,
+                          colsum, B, H, N, inv, out);
 }
 
 bool salience_head_dim_supported(int d) { return d == 64 || d == 72 || d == 80 || d == 128; }

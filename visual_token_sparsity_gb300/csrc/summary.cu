@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kSumThreads, kOneRow ? 8 : 1)
 summary_colsum_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, int N, int d, int R,
                       float sl2, float* __restrict__ colsum) {
   extern __shared__ float sm[];
+  grid_dep_sync();
   float* qs = sm;                       // [R][d], scaled by scale * log2(e)
   float* z = qs + (size_t)R * d;        // [R][N] logits, log2 domain
   float* lse = z + (size_t)R * N;       // [R]
@@ -131,10 +132,9 @@ cudaError_t launch_summary_salience(const void* q, const void* k, int B, int H, 
     if (e != cudaSuccess) return e;
   }
   auto kern = R == 1 ? summary_colsum_kernel<true> : summary_colsum_kernel<false>;
-  kern<<<(unsigned)units, kSumThreads, smem, stream>>>(static_cast<const uint16_t*>(q),
-                                                        static_cast<const uint16_t*>(k), N, d, R, scale * kLog2e,
-                                                        colsum);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(kern, dim3((unsigned)units), dim3(kSumThreads), smem, stream,
+                                   static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), N, d, R,
+                                   scale * kLog2e, colsum);
   if (e != cudaSuccess) return e;
   return launch_head_mean(colsum, B, H, N, 1.0f / ((float)H * (float)R), salience, stream);
 }
