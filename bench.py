@@ -279,6 +279,9 @@ class DecodeWorkload:
 
 
 def time_graph(fn, steps, warmup, stream):
+    # the side stream starts after everything already queued on the current
+    # stream (inputs drawn, outputs allocated from memory it may still read)
+    stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for _ in range(max(1, warmup)):
             fn()
@@ -346,6 +349,7 @@ def e2e_throughput(wl, steps, warmup, stream, bytes_step):
             wl.attend(l, dq_dec[l])
         hout.copy_(wl.out, non_blocking=True)
 
+    stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             one()
@@ -385,6 +389,7 @@ def salience_measure(batch, steps, warmup, stream, tiny=False, shape=None):
     qs = [q] + [q.clone() for _ in range(ncopy - 1)]
     ks = [k] + [k.clone() for _ in range(ncopy - 1)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for i in range(warmup):
             sv.sv_salience_prefill(qs[i % ncopy], ks[i % ncopy], 1 / math.sqrt(ss.d), sal, ws)
@@ -411,6 +416,7 @@ def prune_measure(batch, steps, stream, pk):
     sal = torch.empty(B, N, device="cuda")
     ws = sv.workspace(max(sv.sv_salience_workspace_bytes(B, ss.H, N, ss.d), sv.sv_prune_workspace_bytes(B, N, N)))
     sv.sv_salience_prefill(q, k, 1 / math.sqrt(ss.d), sal, ws)
+    torch.cuda.synchronize()     # q and k are read until here
     del q, k
     kept = torch.empty(B, ss.k, dtype=torch.int32, device="cuda")
     fout = torch.empty(B, ss.k, C, dtype=torch.bfloat16, device="cuda")
