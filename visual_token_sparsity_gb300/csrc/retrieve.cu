@@ -62,7 +62,7 @@ retrieve_score_kernel(const uint16_t* __restrict__ q, int R, int H, int G,
   constexpr int NL = kBlockTokens / TPI;  // loads per lane per page
   static_assert(NL * 2 == LPT, "page fold assumes two lanes per reduced value");
 
-  extern __shared__ uint32_t topk_keys[];
+  extern __shared__ __align__(16) uint32_t topk_keys[];
   __shared__ float qbar[D];
   __shared__ TopkShared ts;
   __shared__ int s_last;

@@ -15,7 +15,7 @@ namespace sv {
 __global__ void __launch_bounds__(1024)
 topk_rows_kernel(const float* __restrict__ scores, int n, int k, int32_t* __restrict__ idx,
                  int keys_in_smem, SeqLens lens, int rows_per_seq) {
-  extern __shared__ uint32_t smem_keys[];
+  extern __shared__ __align__(16) uint32_t smem_keys[];
   __shared__ TopkShared ts;
   grid_dep_sync();
   const int row = blockIdx.x;
