@@ -171,7 +171,13 @@ cudaError_t launch_retrieve(const void* q, int R, int H, int G, const void* k_po
   const long long target = (long long)num_sms * SV_RET_WAVES;
   long long chunks = (target + rows - 1) / rows;
   int per = (int)((n_vblocks + chunks - 1) / chunks);
-  if (per < 8) per = 8;
+  // whole pages per warp (a multiple of the CTA's warps), so that every warp
+  // of a CTA streams the same number of pages: rounded down, at least one
+  // page per warp (measured against the unrounded split: LLaVA-NeXT B16 step
+  // 4.572 -> 4.533 ms, B4 1.709 -> 1.662 ms, LongVILA B8 3.722 -> 3.710 ms)
+  constexpr int kW = kRetrieveThreads / 32;
+  per = per / kW * kW;
+  if (per < kW) per = kW;
   if (per > n_vblocks) per = n_vblocks;
   const int grid_x = (n_vblocks + per - 1) / per;
   const bool fuse = row_done != nullptr && retrieve_fuses_topk(rows, n_vis);
