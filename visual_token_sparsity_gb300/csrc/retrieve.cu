@@ -33,7 +33,7 @@ namespace sv {
 #define SV_RET_THREADS 256
 #endif
 #ifndef SV_RET_WAVES
-#define SV_RET_WAVES 16        // target CTAs = SMs x this
+#define SV_RET_WAVES 20        // target CTAs = SMs x this (12 / 16 / 20 / 24 / 32 measured: 20 best)
 #endif
 #ifndef SV_RET_MINB
 #define SV_RET_MINB 5          // register cap: 5 resident CTAs (40 warps) per SM
