@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256)
 kv_move_down_kernel(uint4* k_pool, uint4* v_pool, int num_blocks, int Hkv, int vecs_per_tok,
                     const int32_t* __restrict__ block_table, int max_blocks, int dst_pos,
                     int src_pos, int count, int* status) {
+  grid_dep_sync();
   const int g = blockIdx.x, b = blockIdx.y;
   const int32_t* bt = block_table + (size_t)b * max_blocks;
   const int shift = src_pos - dst_pos;
@@ -76,11 +77,9 @@ cudaError_t launch_kv_move_down(void* k_pool, void* v_pool, int num_blocks, int 
                                 cudaStream_t stream) {
   if (count <= 0 || batch == 0) return cudaSuccess;
   dim3 grid(Hkv, batch);
-  kv_move_down_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(k_pool),
-                                                static_cast<uint4*>(v_pool), num_blocks, Hkv,
-                                                D / 8, block_table, max_blocks, dst_pos, src_pos,
-                                                count, status);
-  return cudaGetLastError();
+  return launch_dependent(kv_move_down_kernel, grid, dim3(256), 0, stream, static_cast<uint4*>(k_pool),
+                          static_cast<uint4*>(v_pool), num_blocks, Hkv, D / 8, block_table, max_blocks, dst_pos,
+                          src_pos, count, status);
 }
 
 // Writes new tokens' K/V rows ([B][T][Hkv][d], token-major) into their pages,
@@ -92,6 +91,7 @@ kv_append_kernel(uint4* k_pool, uint4* v_pool, int num_blocks, int Hkv, int vecs
                  const int32_t* __restrict__ block_table, int max_blocks, int pos0,
                  const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, int T,
                  long long total, int* status, SeqLens lens, int n_vis, int n_text) {
+  grid_dep_sync();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int v = (int)(i % vecs_per_tok);
@@ -127,11 +127,10 @@ cudaError_t launch_kv_append(void* k_pool, void* v_pool, int num_blocks, int Hkv
   if (total == 0) return cudaSuccess;
   long long blocks = (total + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  kv_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), num_blocks, Hkv, D / 8,
-      block_table, max_blocks, pos0, static_cast<const uint4*>(k_new),
-      static_cast<const uint4*>(v_new), T, total, status, lens, n_vis, n_text);
-  return cudaGetLastError();
+  return launch_dependent(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                          static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), num_blocks, Hkv, D / 8,
+                          block_table, max_blocks, pos0, static_cast<const uint4*>(k_new),
+                          static_cast<const uint4*>(v_new), T, total, status, lens, n_vis, n_text);
 }
 
 }  // namespace sv

@@ -26,6 +26,7 @@ pack_kv_kernel(const uint4* __restrict__ k_src, const uint4* __restrict__ v_src,
                const int32_t* __restrict__ vis_idx, int k, int n_text, uint4* __restrict__ k_dst,
                uint4* __restrict__ v_dst, int dst_blocks, const int32_t* __restrict__ dst_bt,
                int dst_max_blocks, int Hkv, int vecs_per_tok, int* status) {
+  grid_dep_sync();
   const int g = blockIdx.y, b = blockIdx.z;
   const int t0 = blockIdx.x * kPackTokens;
   const int n_tok = k + n_text;
@@ -68,11 +69,10 @@ cudaError_t launch_pack_kv(const void* k_src, const void* v_src, int src_blocks,
   const int n_tok = k + n_text;
   if (batch == 0 || n_tok == 0) return cudaSuccess;
   dim3 grid((n_tok + kPackTokens - 1) / kPackTokens, Hkv, batch);
-  pack_kv_kernel<<<grid, kPackThreads, 0, stream>>>(
-      static_cast<const uint4*>(k_src), static_cast<const uint4*>(v_src), src_blocks, src_bt, src_max_blocks,
-      n_vis, vis_idx, k, n_text, static_cast<uint4*>(k_dst), static_cast<uint4*>(v_dst), dst_blocks, dst_bt,
-      dst_max_blocks, Hkv, D / 8, status);
-  return cudaGetLastError();
+  return launch_dependent(pack_kv_kernel, grid, dim3(kPackThreads), 0, stream, static_cast<const uint4*>(k_src),
+                          static_cast<const uint4*>(v_src), src_blocks, src_bt, src_max_blocks, n_vis, vis_idx, k,
+                          n_text, static_cast<uint4*>(k_dst), static_cast<uint4*>(v_dst), dst_blocks, dst_bt,
+                          dst_max_blocks, Hkv, D / 8, status);
 }
 
 }  // namespace sv
