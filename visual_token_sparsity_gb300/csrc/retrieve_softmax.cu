@@ -73,6 +73,7 @@ struct RsArgs {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kRsWarps * 32)
 retrieve_softmax_kernel(RsArgs a) {
+  grid_dep_sync();
   constexpr int KSTEPS = D / 16;
   constexpr int TILE_BYTES = kRsSub * D * 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -264,6 +265,7 @@ retrieve_softmax_kernel(RsArgs a) {
 // caller's natural-log lse [B][R][H]; padding rows get +inf (no mass).
 __global__ void retrieve_softmax_lse_kernel(const float* __restrict__ part_ml, int nsplit, const float* __restrict__ lse_in,
                                             int R, int H, int G, int Hkv, int RG, int MT, float* __restrict__ lse2) {
+  grid_dep_sync();
   const int unit = blockIdx.x;
   const int b = unit / Hkv, g = unit % Hkv;
   for (int row = threadIdx.x; row < MT * 16; row += blockDim.x) {
@@ -358,26 +360,26 @@ cudaError_t launch_retrieve_softmax(const void* q, int R, int H, float scale, co
     a.chunk = p1.chunk; a.csplit = p1.csplit;
     if (D == 128) {
       if ((e = set_smem((const void*)retrieve_softmax_kernel<128, 0>)) != cudaSuccess) return e;
-      retrieve_softmax_kernel<128, 0><<<units * p1.csplit, kRsWarps * 32, smem, stream>>>(a);
+      e = launch_dependent(retrieve_softmax_kernel<128, 0>, dim3(units * p1.csplit), dim3(kRsWarps * 32), smem, stream, a);
     } else {
       if ((e = set_smem((const void*)retrieve_softmax_kernel<64, 0>)) != cudaSuccess) return e;
-      retrieve_softmax_kernel<64, 0><<<units * p1.csplit, kRsWarps * 32, smem, stream>>>(a);
+      e = launch_dependent(retrieve_softmax_kernel<64, 0>, dim3(units * p1.csplit), dim3(kRsWarps * 32), smem, stream, a);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
   }
-  retrieve_softmax_lse_kernel<<<units, 256, 0, stream>>>(part_ml, p1.csplit * kRsWarps, lse_in, R, H, G, Hkv, RG, MT,
-                                                           lse2);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_dependent(retrieve_softmax_lse_kernel, dim3(units), dim3(256), 0, stream, part_ml, p1.csplit * kRsWarps,
+                       lse_in, R, H, G, Hkv, RG, MT, lse2);
+  if (e != cudaSuccess) return e;
   const RsPlan p2 = rs_plan(units, n_vis);
   a.chunk = p2.chunk; a.csplit = p2.csplit;
   if (D == 128) {
     if ((e = set_smem((const void*)retrieve_softmax_kernel<128, 1>)) != cudaSuccess) return e;
-    retrieve_softmax_kernel<128, 1><<<units * p2.csplit, kRsWarps * 32, smem, stream>>>(a);
+    e = launch_dependent(retrieve_softmax_kernel<128, 1>, dim3(units * p2.csplit), dim3(kRsWarps * 32), smem, stream, a);
   } else {
     if ((e = set_smem((const void*)retrieve_softmax_kernel<64, 1>)) != cudaSuccess) return e;
-    retrieve_softmax_kernel<64, 1><<<units * p2.csplit, kRsWarps * 32, smem, stream>>>(a);
+    e = launch_dependent(retrieve_softmax_kernel<64, 1>, dim3(units * p2.csplit), dim3(kRsWarps * 32), smem, stream, a);
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   if (topk_prefers_cluster(n_vis)) return launch_topk_cluster(scores, units, n_vis, k, vis_idx, stream);
   return launch_topk_rows(scores, units, n_vis, k, vis_idx, stream);
 }
