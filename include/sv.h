@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
   SV_OK = 0,
   SV_ERR_INVALID_ARG = 1,   /* a null pointer, a size out of range, k > n ... */
-  SV_ERR_UNSUPPORTED = 2,   /* a head_dim or shape this build has no kernel for */
+  SV_ERR_UNSUPPORTED = 2,   /* a head_dim or shape the library has no kernel for */
   SV_ERR_CUDA = 3,          /* a CUDA runtime error while launching */
   SV_ERR_WORKSPACE = 4,     /* ws_bytes smaller than required */
   SV_ERR_DEVICE_BOUNDS = 5  /* reported by sv_read_device_status only */
