@@ -464,28 +464,35 @@ salience_kernel(const __grid_constant__ CUtensorMap tq_main, const __grid_consta
     // registers) on each 32-column group of the warp's slice, one group in
     // registers at a time (a single 64-column load, or releasing the buffer
     // before the math, measured slower).
+    // Every chunk but the last has 256 columns (two groups per slice, no key
+    // past N); the last chunk's group count per slice is fixed per launch.
+    static_assert(kBufs == 2, "the chunk counter's low bit is the buffer");
+    const int nc_last = min(kWarpCols, a.Np - kBufCols * (nch - 1) - col_lo);
+    const int ng_last = nc_last > 0 ? nc_last >> 5 : 0;
     auto run_tile = [&](bool live, auto&& fn) {
-      for (int c = 0; c < nch; ++c, ++u) {
-        const uint32_t b = u % kBufs;
-        wait_bar(&sh.bar_full[b], (u / kBufs) & 1, sh);
+      auto chunk = [&](int c, int ng, bool last) {
+        const uint32_t b = u & 1u;
+        wait_bar(&sh.bar_full[b], (u >> 1) & 1u, sh);
         ptx::tc_fence_after();
         const uint32_t taddr = tlane + b * kBufCols;
-        const int nc = min(kWarpCols, a.Np - kBufCols * c - col_lo);
-        const int ng = live && nc > 0 ? nc >> 5 : 0;
         if (ng > 0) {
           ptx::tmem_ld32(taddr, v);
           ptx::tmem_wait_ld(v);
-          fn(c, 0, v);
+          fn(c, 0, v, last);
         }
         if (ng > 1) {
           ptx::tmem_ld32(taddr + 32, v);
           ptx::tmem_wait_ld(v);
-          fn(c, 32, v);
+          fn(c, 32, v, last);
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh.bar_empty[b]);
-      }
+        ++u;
+      };
+      const int ng_full = live ? 2 : 0;
+      for (int c = 0; c < nch - 1; ++c) chunk(c, ng_full, false);
+      chunk(nch - 1, live ? ng_last : 0, true);
     };
     // sum of exp2(sl2 * r) over a group, into the packed accumulator (all on
     // MUFU: moving a share of the exps to an FMA-pipe polynomial measured
@@ -510,8 +517,8 @@ salience_kernel(const __grid_constant__ CUtensorMap tq_main, const __grid_consta
       const bool live = t * kTileRows + quarter * 32 < a.N;
       if (!EXACT) {
         uint64_t acc = 0;
-        run_tile(live, [&](int c, int gofs, uint32_t* r) {
-          mask_keys(kBufCols * c + col_lo + gofs, r);
+        run_tile(live, [&](int c, int gofs, uint32_t* r, bool last) {
+          if (last) mask_keys(kBufCols * c + col_lo + gofs, r);
           sum_exp(acc, r);
         });
         float l0, l1;
@@ -520,8 +527,8 @@ salience_kernel(const __grid_constant__ CUtensorMap tq_main, const __grid_consta
       } else {
         float m = -INFINITY;
         uint64_t l2 = 0;
-        run_tile(live, [&](int c, int gofs, uint32_t* r) {
-          mask_keys(kBufCols * c + col_lo + gofs, r);
+        run_tile(live, [&](int c, int gofs, uint32_t* r, bool last) {
+          if (last) mask_keys(kBufCols * c + col_lo + gofs, r);
           float mx[11];
 #pragma unroll
           for (int i = 0; i < 10; ++i)
@@ -554,7 +561,7 @@ salience_kernel(const __grid_constant__ CUtensorMap tq_main, const __grid_consta
     auto tile_cols = [&](int t) -> float {
       const bool live = t * kTileRows + quarter * 32 < a.N;
       uint64_t acc = 0;
-      run_tile(live, [&](int, int, uint32_t* r) { sum_exp(acc, r); });
+      run_tile(live, [&](int, int, uint32_t* r, bool) { sum_exp(acc, r); });
       float s0, s1;
       fm::unpack2(acc, s0, s1);
       return s0 + s1;
