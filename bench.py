@@ -792,6 +792,8 @@ def main():
         lv = {}
         for b in (8, 1):
             lv[f"b{b}"] = decode_object(synth.longvila_decode(batch=b), dev, extra_steps, 3, stream, pk)
+        # a short video on the same model: 16 frames (3136 visual tokens), batch 16
+        lv["b16_f16"] = decode_object(synth.longvila_decode(batch=16, frames=16), dev, extra_steps, 3, stream, pk)
         line["longvila"] = lv
         # the other LLaVA-NeXT-7B cases: 25% keep at batch 16, batches 4 and 1
         ln = {"b16_keep0.25": decode_object(synth.llava_next_decode(batch=16, keep=0.25), dev, extra_steps, 3,

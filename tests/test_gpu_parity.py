@@ -266,6 +266,8 @@ def test_retrieve_rows_equal_presummed_row(lib):
     (16, 1, 64, 300, 17, 2, 77, True),      # 16 heads per KV head (tensor-core tiles, no padding rows)
     (12, 1, 128, 500, 40, 1, 200, False),   # 12 heads per KV head
     (28, 4, 128, 50176, 256, 1, 12544, True),  # LongVILA shape, one sequence
+    (28, 4, 128, 3136, 256, 4, 784, True),     # LongVILA at 16 frames: 32-token splits, merge kernel
+    (96, 32, 64, 12000, 100, 2, 9600, True),   # G 3, 64 units: 400-token splits (4 row-id blocks a warp)
     # the CUDA-core kernel steps 32 tokens per warp for at most 8 (sequence,
     # KV head) units and 8 tokens above: both sides of that switch, G 1 and 2
     (8, 8, 128, 2880, 128, 1, 721, True),     # 8 units, G 1

@@ -53,8 +53,35 @@ constexpr int kAttnWarps = 4;
 #define SV_ATTN_TARGET_WARPS 4096   // <= 152 SMs x 7 CTAs x 4 warps: one wave
 #endif
 constexpr int kAttnTargetWarps = SV_ATTN_TARGET_WARPS;
+// Tensor-core kernel (G >= 3) split plan: at most kMmaTargetWarps warps in
+// all (152 SMs x 3 CTAs x 4 warps = 1824 resident; 1600 keeps LongVILA-sized
+// calls at 256-token splits, measured faster than 240), at least
+// kMmaMinTokens tokens and at most kMmaMaxSplits splits per (sequence, KV
+// head): short calls gain from many short splits, while above ~200 splits
+// the merge kernel's per-split loads cost more than the extra warps save.
+#ifndef SV_MMA_TARGET_WARPS
+#define SV_MMA_TARGET_WARPS 1600
+#endif
+#ifndef SV_MMA_MIN_TOKENS
+#define SV_MMA_MIN_TOKENS 32
+#endif
+#ifndef SV_MMA_MAX_SPLITS
+#define SV_MMA_MAX_SPLITS 200
+#endif
+constexpr int kMmaTargetWarps = SV_MMA_TARGET_WARPS;
+constexpr int kMmaMinTokens = SV_MMA_MIN_TOKENS;
+constexpr int kMmaMaxSplits = SV_MMA_MAX_SPLITS;
 constexpr int kAttnMaxSplits = 1024;
 constexpr int kFusedMergeMaxSplits = 32;   // above this a separate merge kernel runs
+#ifndef SV_MMA_FUSED_MAX
+#define SV_MMA_FUSED_MAX 0
+#endif
+// Tensor-core kernel: its last warp would merge G heads x nsplit partial rows
+// one after another, which measured slower than the merge kernel at every
+// size tried (G 7 with 7-28 splits: 31.4 against 22.3 us for 16 sequences of
+// 1568 tokens), so by default (a product bound of 0) that path always runs
+// the merge kernel.
+constexpr int kMmaFusedMergeMax = SV_MMA_FUSED_MAX;
 constexpr uint32_t kNoRow = 0xffffffffu;
 
 // tokens per warp step: one 16-token MMA sub-tile for the tensor-core kernel
@@ -76,17 +103,20 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   p.tile = attn_tile(G, units);
   const int tiles = (n_tokens + p.tile - 1) / p.tile;
   long long tiles_total = units * (tiles > 0 ? tiles : 1);
-  long long tpw = (tiles_total + kAttnTargetWarps - 1) / kAttnTargetWarps;
-  if (tpw < 1) tpw = 1;
-  long long min_tpw = (tiles + kAttnMaxSplits - 1) / kAttnMaxSplits;
-  if (tpw < min_tpw) tpw = min_tpw;
-  // small tiles (large G): at least 128 tokens per split, or the partials
-  // (G x (d + 2) floats per split) and their merge dominate; with 16 or more
-  // (sequence, KV head) units there is parallelism enough for 256, which
-  // halves each warp's share of fixed costs (row-id resolution, pipeline
-  // fill, partial write)
-  const long long min_tokens = attn_uses_mma(G) ? (units >= 16 ? 256 : 128) : 0;
-  if (tpw * p.tile < min_tokens) tpw = (min_tokens + p.tile - 1) / p.tile;
+  long long tpw;
+  if (attn_uses_mma(G)) {
+    long long cap = kMmaTargetWarps / (units > 0 ? units : 1);
+    if (cap > kMmaMaxSplits) cap = kMmaMaxSplits;
+    if (cap < 1) cap = 1;
+    tpw = ((tiles > 0 ? tiles : 1) + cap - 1) / cap;
+    const long long min_tpw = (kMmaMinTokens + p.tile - 1) / p.tile;
+    if (tpw < min_tpw) tpw = min_tpw;
+  } else {
+    tpw = (tiles_total + kAttnTargetWarps - 1) / kAttnTargetWarps;
+    if (tpw < 1) tpw = 1;
+    const long long min_tpw = (tiles + kAttnMaxSplits - 1) / kAttnMaxSplits;
+    if (tpw < min_tpw) tpw = min_tpw;
+  }
   // CUDA-core path: stay within the fused merge (at most kFusedMergeMaxSplits
   // splits, merged by the last warp) when that still leaves 512 or more warps;
   // a separate merge launch costs more than longer splits at small batches
@@ -99,21 +129,26 @@ AttnPlan attn_plan(int B, int Hkv, int G, int n_tokens) {
   // nsplit <= ceil(tiles / tpw) <= min(tiles, ceil(target / units), max): a
   // bound that never decreases as n_tokens grows (workspace sizing).
   // chunk >= max(tile, min_tokens), so nsplit <= ceil(n_tokens / that)
-  // (the bound takes the smaller split minimum, 128, whatever `units` is)
-  const long long min_bound_tokens = attn_uses_mma(G) ? 128 : 0;
   const long long min_chunk =
-      min_bound_tokens > p.tile ? (min_bound_tokens + p.tile - 1) / p.tile * p.tile : p.tile;
+      attn_uses_mma(G) && kMmaMinTokens > p.tile ? (kMmaMinTokens + p.tile - 1) / p.tile * p.tile : p.tile;
   long long ub = (n_tokens + min_chunk - 1) / min_chunk;
   if (ub < 1) ub = 1;
-  const long long per_unit = (kAttnTargetWarps + units - 1) / (units > 0 ? units : 1);
+  const long long target = attn_uses_mma(G) ? kMmaTargetWarps : kAttnTargetWarps;
+  const long long per_unit = (target + units - 1) / (units > 0 ? units : 1);
   if (ub > per_unit) ub = per_unit;
   if (ub > kAttnMaxSplits) ub = kAttnMaxSplits;
+  if (attn_uses_mma(G) && ub > kMmaMaxSplits) ub = kMmaMaxSplits;
   p.nsplit_max = (int)(ub > p.nsplit ? ub : p.nsplit);
   return p;
 }
 
+static bool attn_fused_merge(const AttnPlan& p, int G) {
+  if (p.nsplit > kFusedMergeMaxSplits) return false;
+  return !attn_uses_mma(G) || (long long)G * p.nsplit <= kMmaFusedMergeMax;
+}
+
 int attn_kernel_count(int B, int Hkv, int G, int n_tokens) {
-  return attn_plan(B, Hkv, G, n_tokens).nsplit <= kFusedMergeMaxSplits ? 1 : 2;
+  return attn_fused_merge(attn_plan(B, Hkv, G, n_tokens), G) ? 1 : 2;
 }
 
 template <int D, int G, int TILE_>
@@ -440,7 +475,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.H / a.Hkv;
   const AttnPlan p = attn_plan(a.batch, a.Hkv, G, a.k_vis + a.n_text);
   AttnArgs b = a;
-  const bool fused_merge = p.nsplit <= kFusedMergeMaxSplits;
+  const bool fused_merge = attn_fused_merge(p, G);
   if (!fused_merge) b.split_done = nullptr;
   cudaError_t e;
   if (attn_uses_mma(G)) {

@@ -19,11 +19,17 @@ namespace sv {
 
 namespace {
 
-constexpr int kMmaWarps = 4;
+#ifndef SV_MMA_WARPS
+#define SV_MMA_WARPS 4
+#endif
+#ifndef SV_MMA_STAGES
+#define SV_MMA_STAGES 2
+#endif
+constexpr int kMmaWarps = SV_MMA_WARPS;
 // Two stages (one sub-tile in flight while the previous one is processed):
 // 64 KB of shared memory per 4-warp CTA, so three CTAs fit an SM; more
 // resident warps measured faster than a deeper ring with two CTAs per SM.
-constexpr int kMmaStages = 2;
+constexpr int kMmaStages = SV_MMA_STAGES;
 constexpr int kSubTile = 16;      // tokens per MMA step
 constexpr uint32_t kNoRowM = 0xffffffffu;
 
@@ -145,33 +151,49 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
 
   const int nsub = (t_end - t_begin + kSubTile - 1) / kSubTile;
   uint32_t rows[kMmaStages];
-  // Row ids of a block of 128 tokens (8 sub-tiles) are resolved together, the
-  // next block's while the current one streams: the index and page-table
-  // loads cost two dependent round trips per block, not per sub-tile.
-  uint32_t blk_cur[4] = {kNoRowM, kNoRowM, kNoRowM, kNoRowM}, blk_next[4] = {kNoRowM, kNoRowM, kNoRowM, kNoRowM};
-  auto resolve_block = [&](int t0, uint32_t* r) {
+  // Row ids of 128-token blocks (8 sub-tiles) come through a software
+  // pipeline: a block's visual indices are loaded two blocks ahead, its
+  // page-table entries one block ahead, and its row ids are formed when its
+  // first sub-tile is issued, so neither dependent round trip stalls the
+  // stream (only the first block's two wait, before the first copy).
+  int pos_a[4], pg_a[4];                  // block j + 1: checked positions, pages in flight
+  int pos_b[4];                           // block j + 2: raw visual indices in flight
+  uint32_t blk_cur[4];                    // block j: row ids
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) { pos_a[q4] = pg_a[q4] = pos_b[q4] = -1; blk_cur[q4] = kNoRowM; }
+  auto load_idx = [&](int t0, int* p) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int tok = t0 + 32 * q4 + lane;
+      p[q4] = (vrow != nullptr && tok < t_end && tok < kb) ? __ldg(vrow + tok) : -1;
+    }
+  };
+  // checks the positions of the block at t0 and issues its page-table loads
+  auto load_pages = [&](int t0, int* p, int* pg) {
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       const int tok = t0 + 32 * q4 + lane;
       int pos = -1;
       if (tok < t_end) {
         if (tok < kb) {
-          pos = vrow ? __ldg(vrow + tok) : tok;
+          pos = vrow ? p[q4] : tok;
           if (pos < 0 || pos >= nv) { flag_status(status, kStatusBadIndex); pos = -1; }
         } else {
           pos = nv + (tok - kb);
         }
       }
-      r[q4] = (uint32_t)pos;
+      p[q4] = pos;
+      pg[q4] = pos >= 0 ? __ldg(bt + (pos >> 4)) : -1;
     }
+  };
+  auto form_rows = [&](const int* p, const int* pg, uint32_t* r) {
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
-      const int pos = (int)r[q4];
       uint32_t rid = kNoRowM;
-      if (pos >= 0) {
-        const int page = __ldg(bt + (pos >> 4));
+      if (p[q4] >= 0) {
+        const int page = pg[q4];
         if (page >= 0 && page < num_blocks)
-          rid = (((uint32_t)page * (uint32_t)Hkv + (uint32_t)g) << 4) | (uint32_t)(pos & 15);
+          rid = (((uint32_t)page * (uint32_t)Hkv + (uint32_t)g) << 4) | (uint32_t)(p[q4] & 15);
         else
           flag_status(status, kStatusBadBlock);
       }
@@ -184,8 +206,15 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
     const uint32_t v = q4 == 0 ? blk_cur[0] : q4 == 1 ? blk_cur[1] : q4 == 2 ? blk_cur[2] : blk_cur[3];
     return __shfl_sync(0xffffffffu, v, (lane & 15) + 16 * (i & 1));
   };
-  resolve_block(t_begin, blk_cur);
-  if (nsub > 8) resolve_block(t_begin + 128, blk_next);
+  {
+    int pos0[4], pg0[4];
+    load_idx(t_begin, pos0);
+    if (nsub > 8) load_idx(t_begin + 128, pos_a);
+    if (nsub > 16) load_idx(t_begin + 256, pos_b);
+    load_pages(t_begin, pos0, pg0);
+    if (nsub > 8) load_pages(t_begin + 128, pos_a, pg_a);
+    form_rows(pos0, pg0, blk_cur);
+  }
 #pragma unroll
   for (int s = 0; s < kMmaStages - 1; ++s) {
     if (s < nsub) rows[s] = issue(t_begin + s * kSubTile, s, rows_of(s));
@@ -198,9 +227,13 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
     const int nxt = it + kMmaStages - 1;
     if (nxt < nsub) {
       if ((nxt & 7) == 0) {       // first sub-tile of a new 128-token block
+        form_rows(pos_a, pg_a, blk_cur);
+        if (nxt + 8 < nsub) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) blk_cur[q4] = blk_next[q4];
-        if (nxt + 8 < nsub) resolve_block(t_begin + (nxt + 8) * kSubTile, blk_next);
+          for (int q4 = 0; q4 < 4; ++q4) pos_a[q4] = pos_b[q4];
+          load_pages(t_begin + (nxt + 8) * kSubTile, pos_a, pg_a);
+        }
+        if (nxt + 16 < nsub) load_idx(t_begin + (nxt + 16) * kSubTile, pos_b);
       }
       rows[nxt % kMmaStages] = issue(t_begin + nxt * kSubTile, nxt % kMmaStages, rows_of(nxt));
     } else {

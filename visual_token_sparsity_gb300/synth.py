@@ -184,9 +184,10 @@ def qwen2vl_salience(batch=1, N=16384, keep=0.25):
                          std=1.0 / math.sqrt(80.0), seed=7)
 
 
-def longvila_decode(batch=1, layers=28):
-    """Qwen2-7B attention (28 q heads, 4 KV heads, d 128), 256x196 visual + 256 text."""
-    return DecodeShape("longvila-7b-decode", H=28, Hkv=4, d=128, n_vis=50176, n_text=256,
+def longvila_decode(batch=1, layers=28, frames=256):
+    """Qwen2-7B attention (28 q heads, 4 KV heads, d 128), frames x 196 visual
+    (256 frames: 50176) + 256 text."""
+    return DecodeShape("longvila-7b-decode", H=28, Hkv=4, d=128, n_vis=196 * frames, n_text=256,
                        layers=layers, batch=batch, keep=0.25, R=1, v_outliers=False, seed=3)
 
 
