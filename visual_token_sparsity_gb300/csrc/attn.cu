@@ -54,13 +54,12 @@ constexpr int kAttnWarps = 4;
 #endif
 constexpr int kAttnTargetWarps = SV_ATTN_TARGET_WARPS;
 // Tensor-core kernel (G >= 3) split plan: at most kMmaTargetWarps warps in
-// all (152 SMs x 3 CTAs x 4 warps = 1824 resident; 1600 keeps LongVILA-sized
-// calls at 256-token splits, measured faster than 240), at least
+// all (152 SMs x 4 CTAs x 2 warps resident: one wave), at least
 // kMmaMinTokens tokens and at most kMmaMaxSplits splits per (sequence, KV
 // head): short calls gain from many short splits, while above ~200 splits
 // the merge kernel's per-split loads cost more than the extra warps save.
 #ifndef SV_MMA_TARGET_WARPS
-#define SV_MMA_TARGET_WARPS 1600
+#define SV_MMA_TARGET_WARPS 1216
 #endif
 #ifndef SV_MMA_MIN_TOKENS
 #define SV_MMA_MIN_TOKENS 32
