@@ -31,15 +31,6 @@ constexpr int kRsMaxRows = 256;     // R * G
 constexpr int kRsTargetWarps = 4096;
 constexpr uint32_t kNoRowRs = 0xffffffffu;
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
@@ -156,9 +147,9 @@ retrieve_softmax_kernel(RsArgs a) {
       issue(s ^ 1, rid_next);
       rid_cur = rid_next;
       if (it + 2 < nsub) rid_next = resolve(t_begin + (it + 2) * kRsSub);
-      cp_async_wait1();
+      cp_async_wait<1>();
     } else {
-      cp_async_wait0();
+      cp_async_wait<0>();
     }
     __syncwarp();
     const uint32_t kbase = smem_u32(my + (size_t)s * TILE_BYTES);
