@@ -342,21 +342,34 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   constexpr int DPL = D / 32;   // output dims per lane
   const size_t base = (size_t)bg * nsplit;
   for (int hh = 0; hh < G; ++hh) {
-    float M = -INFINITY;
-    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, __ldcg(part_ml + ((base + s) * G + hh) * 2));
-    M = warp_max(M);
-    float L = 0.f, acc[DPL];
+    // lane s holds split s (nsplit <= 32 here): its (m, l) and weight come in
+    // one round of loads; the partial rows follow kMergeBatch splits at a time
+    float ms = -INFINITY, ls = 0.f;
+    if (lane < nsplit) {
+      ms = __ldcg(part_ml + ((base + lane) * G + hh) * 2);
+      ls = __ldcg(part_ml + ((base + lane) * G + hh) * 2 + 1);
+    }
+    const float M = warp_max(ms);
+    const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
+    const float L = warp_sum(w * ls);
+    float acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < nsplit; ++s) {
-      const size_t ps = (base + s) * G + hh;
-      const float ms = __ldcg(part_ml + ps * 2);
-      const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
-      L = fmaf(w, __ldcg(part_ml + ps * 2 + 1), L);
-      const float* po = part_o + ps * D + lane * DPL;
+    constexpr int kMergeBatch = 8;
+    for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+      float x[kMergeBatch][DPL];
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(w, __ldcg(po + e), acc[e]);
+      for (int j = 0; j < kMergeBatch; ++j) {
+        const float* po = part_o + ((base + s0 + j) * G + hh) * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) x[j][e] = s0 + j < nsplit ? __ldcg(po + e) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, s0 + j);   // 0 past nsplit
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wj, x[j][e], acc[e]);
+      }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint16_t* dst = out + ((size_t)b * H + g * G + hh) * D + lane * DPL;
