@@ -639,16 +639,37 @@ def rounds_measure(batch, steps, warmup, stream):
             pseqs.n_text += 1
             sv.sv_sparse_decode_attn(aq[t], scale, player, pseqs, None, 0, outs_p[t], None, ws_a)
 
+    # fused variant: each decode step is one sv_decode_append_attn launch
+    akf = [ak[:, t, 0].contiguous() for t in range(256)]
+    avf = [av[:, t, 0].contiguous() for t in range(256)]
+    outs_f = torch.empty_like(outs)
+
+    def one_round_fused():
+        seqs = sv.SeqBatch(bt, s.n_vis, 32 + 32 + 256)
+        sv.sv_evict_qa_tokens([layer], seqs, 32, seqs.n_text, ws_e)
+        sv.sv_kv_append(layer, seqs, qk, qv, ws_e)
+        seqs.n_text += 32
+        sv.sv_retrieve_topk(rows, layer, seqs, s.k, vis, None, ws_r)
+        for t in range(256):
+            sv.sv_decode_append_attn(aq[t], scale, layer, seqs, akf[t], avf[t], vis, s.k, outs_f[t], None, ws_a)
+            seqs.n_text += 1
+
     graph = time_graph(one_round, steps, max(3, warmup), stream)
     ms = replay_timed(graph, steps, stream, lambda: None)
     graph_p = time_graph(one_round_packed, steps, max(3, warmup), stream)
     ms_p = replay_timed(graph_p, steps, stream, lambda: None)
-    del graph, graph_p
+    graph_f = time_graph(one_round_fused, steps, max(3, warmup), stream)
+    ms_f = replay_timed(graph_f, steps, stream, lambda: None)
+    del graph, graph_p, graph_f
     return {"workload": "round loop: evict, append 32-token question, retrieve top-25% with 32 rows, "
                         "256 x (append + sparse attention); 4 q / 2 KV heads, d 64, 576 visual + 32-token "
                         f"prefix, batch {s.batch}",
             "round_us": ms * 1e3, "per_decode_step_us": ms * 1e3 / 256,
             "rounds_per_s": 1e3 / ms, "gpu_launches_per_round": 1 + 1 + 256 * 2,
+            "fused": {"round_us": ms_f * 1e3, "per_decode_step_us": ms_f * 1e3 / 256,
+                      "gpu_launches_per_round": 1 + 1 + 256,
+                      "note": "same round with each decode step's append and attention in one launch "
+                              "(sv_decode_append_attn)"},
             "packed": {"round_us": ms_p * 1e3, "per_decode_step_us": ms_p * 1e3 / 256,
                        "note": "same round with the selection packed once (sv_pack_kv) and dense "
                                "attention over the packed pages"}}

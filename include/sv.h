@@ -400,6 +400,30 @@ sv_status sv_kv_append(const sv_kv_layer* layer, const sv_seq_batch* seqs, const
                        const void* v_new, int T, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * One decode step of a round in one launch: sv_kv_append(layer, seqs, k_new,
+ * v_new, T = 1, ...) followed by sv_sparse_decode_attn over the selected
+ * visual tokens and the n_text + 1 text tokens (the new token attends to
+ * itself, as the last one).  Same results, bit for bit, as the two calls:
+ * the new token's K and V are read from k_new / v_new and stored into the
+ * cache at position n_vis + n_text (n_vis_seq[b] + n_text_seq[b] with
+ * per-sequence lengths) for later steps; the caller then adds 1 to n_text,
+ * as after sv_kv_append.  (No counterpart on the SparseVILA pages: the
+ * velog.io summary §4.1 round protocol decodes its answer token by token;
+ * fusing the append is a launch saving, not part of the method.)
+ * q, vis_idx, k, out, lse: as for sv_sparse_decode_attn.
+ * k_new, v_new: bf16 [B][Hkv][d], 16-byte aligned; n_vis + n_text + 1 must
+ *               fit in max_blocks * 16, and the page must be in the table.
+ * ws      : sv_attn_workspace_bytes(B, H, n_kv_heads, d, k + n_text + 1)
+ *           (k = n_vis when vis_idx is NULL).
+ * A block id outside the pool is reported (SV_DEV_BAD_BLOCK) and the new
+ * token is then neither stored nor attended, as with the two calls.
+ */
+sv_status sv_decode_append_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
+                                const sv_seq_batch* seqs, const void* k_new, const void* v_new,
+                                const int32_t* vis_idx, int k, void* out, float* lse, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/*
  * Read (and optionally clear) the device status word of a workspace.
  * Synchronises `stream`.  status_out: host int32 (SV_DEV_* bits, 0 = clean).
  */

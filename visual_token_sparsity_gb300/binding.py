@@ -65,6 +65,8 @@ _SIGS = {
                                       ctypes.POINTER(sv_seq_batch), _I, _VP, _VP, _VP]),
     "sv_sparse_decode_attn": (_I, [_VP, _I, _F, ctypes.POINTER(sv_kv_layer),
                                    ctypes.POINTER(sv_seq_batch), _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
+    "sv_decode_append_attn": (_I, [_VP, _I, _F, ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch),
+                                   _VP, _VP, _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
     "sv_evict_qa_tokens": (_I, [ctypes.POINTER(sv_kv_layer), _I, ctypes.POINTER(sv_seq_batch),
                                 ctypes.c_int32, ctypes.c_int32, _VP, _VP, _SZ, _VP]),
     "sv_kv_append": (_I, [ctypes.POINTER(sv_kv_layer), ctypes.POINTER(sv_seq_batch), _VP, _VP, _I,
@@ -319,6 +321,18 @@ def sv_sparse_decode_attn(q, scale, layer, seqs, vis_idx, k, out, lse, ws, strea
     _check(lib.sv_sparse_decode_attn(_ptr(q, torch.bfloat16, "q"), H, float(scale), ctypes.byref(layer.c),
                                      ctypes.byref(seqs.c), _ptr(vis_idx, torch.int32, "vis_idx"), k,
                                      _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                                     *_ws(ws), _stream(stream)))
+
+
+def sv_decode_append_attn(q, scale, layer, seqs, k_new, v_new, vis_idx, k, out, lse, ws, stream=None):
+    """sv_kv_append of one token (k_new, v_new bf16 [B][Hkv][d]) then sparse attention over it and the
+    cache, in one launch; n_text unchanged (the caller adds 1)."""
+    lib = load()
+    B, H, d = q.shape
+    _check(lib.sv_decode_append_attn(_ptr(q, torch.bfloat16, "q"), H, float(scale), ctypes.byref(layer.c),
+                                     ctypes.byref(seqs.c), _ptr(k_new, torch.bfloat16, "k_new"),
+                                     _ptr(v_new, torch.bfloat16, "v_new"), _ptr(vis_idx, torch.int32, "vis_idx"),
+                                     k, _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
                                      *_ws(ws), _stream(stream)))
 
 

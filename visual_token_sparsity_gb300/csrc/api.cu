@@ -354,9 +354,14 @@ sv_status sv_retrieve_topk_softmax(const void* q, int R, int H, float scale, con
   return cuda_status(e, "sv_retrieve_topk_softmax");
 }
 
-sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
-                                const sv_seq_batch* seqs, const int32_t* vis_idx, int k, void* out,
-                                float* lse, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+// sv_sparse_decode_attn, and with k_new / v_new the fused append of one token
+// per sequence before it (sv_decode_append_attn)
+static sv_status decode_attn(const char* name, const void* q, int H, float scale, const sv_kv_layer* layer,
+                             const sv_seq_batch* seqs, const void* k_new, const void* v_new,
+                             const int32_t* vis_idx, int k, void* out, float* lse, void* ws, size_t ws_bytes,
+                             void* stream) {
   sv_status s = check_cache(layer, seqs, true);
   if (s != SV_OK) return s;
   if (!q || !out) return fail(SV_ERR_INVALID_ARG, "q and out must be non-NULL");
@@ -365,9 +370,17 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
   if (H <= 0 || H % Hkv) return fail(SV_ERR_INVALID_ARG, "H must be a positive multiple of n_kv_heads");
   if (H / Hkv > 16) return fail(SV_ERR_UNSUPPORTED, "query heads per KV head %d > 16", H / Hkv);
   if (!std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale must be finite");
+  const bool append = k_new != nullptr || v_new != nullptr;
+  if (append) {
+    if (!k_new || !v_new) return fail(SV_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+    if (!aligned16(k_new) || !aligned16(v_new))
+      return fail(SV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if ((long long)seqs->n_vis + seqs->n_text + 1 > (long long)seqs->max_blocks * SV_BLOCK_TOKENS)
+      return fail(SV_ERR_INVALID_ARG, "appending a token overflows the block table");
+  }
   const int k_vis = vis_idx ? k : seqs->n_vis;
   if (vis_idx && (k < 0 || k > seqs->n_vis)) return fail(SV_ERR_INVALID_ARG, "need 0 <= k <= n_vis");
-  const int n_tok = k_vis + seqs->n_text;
+  const int n_tok = k_vis + seqs->n_text + (append ? 1 : 0);
   if (n_tok <= 0) return fail(SV_ERR_INVALID_ARG, "the attended token set is empty");
   s = check_ws(ws, ws_bytes, sv_attn_workspace_bytes(seqs->batch, H, Hkv, layer->head_dim, n_tok));
   if (s != SV_OK) return s;
@@ -382,6 +395,7 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
   a.vis_idx = vis_idx; a.k_vis = k_vis; a.n_vis = seqs->n_vis; a.n_text = seqs->n_text;
   a.batch = seqs->batch; a.out = out; a.lse = lse;
   a.lens = lens_of(seqs);
+  a.k_new = k_new; a.v_new = v_new;
   // the counters' offset depends only on the batch shape, so a workspace
   // reused with other token counts finds them where the last call zeroed them
   const size_t cnt_bytes = round256((size_t)seqs->batch * Hkv * sizeof(int));
@@ -389,7 +403,25 @@ sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_l
   a.part_ml = reinterpret_cast<float*>(after_status(ws) + cnt_bytes);
   a.part_o = reinterpret_cast<float*>(after_status(ws) + cnt_bytes + round256(parts * 2 * sizeof(float)));
   a.status = status_word(ws);
-  return cuda_status(sv::launch_sparse_attn(a, static_cast<cudaStream_t>(stream)), "sv_sparse_decode_attn");
+  return cuda_status(sv::launch_sparse_attn(a, static_cast<cudaStream_t>(stream)), name);
+}
+
+extern "C" {
+
+sv_status sv_sparse_decode_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
+                                const sv_seq_batch* seqs, const int32_t* vis_idx, int k, void* out,
+                                float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return decode_attn("sv_sparse_decode_attn", q, H, scale, layer, seqs, nullptr, nullptr, vis_idx, k, out, lse, ws,
+                     ws_bytes, stream);
+}
+
+sv_status sv_decode_append_attn(const void* q, int H, float scale, const sv_kv_layer* layer,
+                                const sv_seq_batch* seqs, const void* k_new, const void* v_new,
+                                const int32_t* vis_idx, int k, void* out, float* lse, void* ws, size_t ws_bytes,
+                                void* stream) {
+  if (!k_new || !v_new) return fail(SV_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+  return decode_attn("sv_decode_append_attn", q, H, scale, layer, seqs, k_new, v_new, vis_idx, k, out, lse, ws,
+                     ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ rounds

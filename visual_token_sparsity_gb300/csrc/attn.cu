@@ -81,7 +81,7 @@ constexpr int kFusedMergeMaxSplits = 32;   // above this a separate merge kernel
 // 1568 tokens), so by default (a product bound of 0) that path always runs
 // the merge kernel.
 constexpr int kMmaFusedMergeMax = SV_MMA_FUSED_MAX;
-constexpr uint32_t kNoRow = 0xffffffffu;
+constexpr uint32_t kNoRow = kNoRowId;
 
 // tokens per warp step: one 16-token MMA sub-tile for the tensor-core kernel
 // (attn_mma.cu, G >= 3); for the CUDA-core kernel (G <= 2) 8-token steps at
@@ -150,7 +150,9 @@ int attn_kernel_count(int B, int Hkv, int G, int n_tokens) {
   return attn_fused_merge(attn_plan(B, Hkv, G, n_tokens), G) ? 1 : 2;
 }
 
-template <int D, int G, int TILE_>
+// APPEND: the fused append-and-attend variant (k_new / v_new set); a separate
+// instantiation, so that the plain call's hot loop carries none of it.
+template <int D, int G, int TILE_, bool APPEND>
 __global__ void __launch_bounds__(kAttnWarps * 32, (G == 1 ? (TILE_ <= 8 ? SV_ATTN_MIN_BLOCKS : 3) : 1))
 sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
                          const uint16_t* __restrict__ k_pool, const uint16_t* __restrict__ v_pool,
@@ -159,7 +161,8 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
                          int n_vis, int n_text, float scale_log2, int batch, int nsplit, int chunk,
                          float* __restrict__ part_ml, float* __restrict__ part_o, int* status,
                          int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse,
-                         SeqLens lens) {
+                         SeqLens lens, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                         uint16_t* k_store, uint16_t* v_store) {
   using S = AttnShape<D, G, TILE_>;
   constexpr int LPT = S::LPT, TPI = S::TPI, TILE = S::TILE, NL = S::NL, DUP = S::DUP;
 
@@ -173,12 +176,17 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   // this sequence's counts (k_vis, n_vis, n_text are capacities with
   // per-sequence lengths; splits past its tokens stay empty)
   int nv, nt, kb;
-  attn_lengths(lens, vis_idx != nullptr, b, n_vis, n_text, k_vis, lane == 0 && split == 0 && g == 0, status,
-               nv, nt, kb);
-  const int T = kb + nt;
+  const bool seq_ok = attn_lengths(lens, vis_idx != nullptr, b, n_vis, n_text, k_vis,
+                                   lane == 0 && split == 0 && g == 0, status, nv, nt, kb);
+  // a fused append adds the new token (cache position nv + nt) as the last one
+  const bool append = APPEND && seq_ok;
+  const int T = kb + nt + (append ? 1 : 0);
   const int t_begin = split * chunk;
   const int t_end = min(T, t_begin + chunk);
   const int dim0 = (lane % LPT) * 8;
+  if (append && split == 0)
+    store_new_token(k_store, v_store, k_new, v_new, block_table + (size_t)b * max_blocks, num_blocks, Hkv, D, b, g,
+                    nv + nt, lane);
 
   float qv[G][8];
 #pragma unroll
@@ -221,8 +229,10 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
   auto lookup = [&](int pos) -> uint32_t {
     if (pos < 0) return kNoRow;
     const int page = __ldg(bt + (pos >> 4));
-    if (page >= 0 && page < num_blocks)
+    if (page >= 0 && page < num_blocks) {
+      if (append && pos == nv + nt) return kNewRowId;   // read from k_new / v_new
       return (((uint32_t)page * (uint32_t)Hkv + (uint32_t)g) << 4) | (uint32_t)(pos & 15);
+    }
     flag_status(status, kStatusBadBlock);
     return kNoRow;
   };
@@ -232,8 +242,9 @@ sparse_attn_split_kernel(const uint16_t* __restrict__ q, int H,
     for (int i = 0; i < NL; ++i) {
       const uint32_t r = __shfl_sync(0xffffffffu, rowid, i * TPI + lane / LPT);
       if (r != kNoRow) {
-        kd[i] = ld_stream16(k_pool + (size_t)r * D + dim0);
-        vd[i] = ld_stream16(v_pool + (size_t)r * D + dim0);
+        const bool fresh = APPEND && r == kNewRowId;
+        kd[i] = ld_stream16((fresh ? k_new + (size_t)bg * D : k_pool + (size_t)r * D) + dim0);
+        vd[i] = ld_stream16((fresh ? v_new + (size_t)bg * D : v_pool + (size_t)r * D) + dim0);
       } else {
         kd[i] = make_uint4(0, 0, 0, 0);
         vd[i] = make_uint4(0, 0, 0, 0);
@@ -385,12 +396,16 @@ template <int D, int G, int TILE>
 static cudaError_t launch_split(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
   const long long warps = (long long)a.batch * a.Hkv * p.nsplit;
   const unsigned grid = (unsigned)((warps + kAttnWarps - 1) / kAttnWarps);
-  return launch_dependent(sparse_attn_split_kernel<D, G, TILE>, dim3(grid), dim3(kAttnWarps * 32), 0, stream,
+  auto kernel = a.k_new != nullptr ? sparse_attn_split_kernel<D, G, TILE, true>
+                                   : sparse_attn_split_kernel<D, G, TILE, false>;
+  return launch_dependent(kernel, dim3(grid), dim3(kAttnWarps * 32), 0, stream,
                           static_cast<const uint16_t*>(a.q), a.H, static_cast<const uint16_t*>(a.k_pool),
                           static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks,
                           a.vis_idx, a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk,
                           a.part_ml, a.part_o, a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse,
-                          a.lens);
+                          a.lens, static_cast<const uint16_t*>(a.k_new), static_cast<const uint16_t*>(a.v_new),
+                          static_cast<uint16_t*>(const_cast<void*>(a.k_pool)),
+                          static_cast<uint16_t*>(const_cast<void*>(a.v_pool)));
 }
 
 template <int D, int G>
@@ -485,7 +500,8 @@ attn_merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ p
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.H / a.Hkv;
-  const AttnPlan p = attn_plan(a.batch, a.Hkv, G, a.k_vis + a.n_text);
+  // a fused append attends one token more
+  const AttnPlan p = attn_plan(a.batch, a.Hkv, G, a.k_vis + a.n_text + (a.k_new != nullptr ? 1 : 0));
   AttnArgs b = a;
   const bool fused_merge = attn_fused_merge(p, G);
   if (!fused_merge) b.split_done = nullptr;

@@ -33,7 +33,7 @@ namespace {
 constexpr int kMmaWarps = SV_MMA_WARPS;
 constexpr int kMmaStages = SV_MMA_STAGES;
 constexpr int kSubTile = 16;      // tokens per MMA step
-constexpr uint32_t kNoRowM = 0xffffffffu;
+constexpr uint32_t kNoRowM = kNoRowId;
 
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -60,7 +60,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // One warp per (sequence, KV head, token split); each warp owns a private
 // kMmaStages-deep ring of K and V sub-tiles in shared memory.
-template <int D>
+// APPEND: the fused append-and-attend variant (k_new / v_new set), a separate
+// instantiation.
+template <int D, bool APPEND>
 __global__ void __launch_bounds__(kMmaWarps * 32)
 sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
                        const uint16_t* __restrict__ k_pool, const uint16_t* __restrict__ v_pool,
@@ -69,7 +71,8 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
                        int n_text, float scale_log2, int batch, int nsplit, int chunk,
                        float* __restrict__ part_ml, float* __restrict__ part_o, int* status,
                        int* split_done, uint16_t* __restrict__ out, float* __restrict__ lse,
-                       SeqLens lens) {
+                       SeqLens lens, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                       uint16_t* k_store, uint16_t* v_store) {
   constexpr int CPR = D / 8;                         // 16-byte chunks per token row
   constexpr int KSTEPS = D / 16;
   constexpr int NT_O = D / 8;                        // output n-tiles (8 dims each)
@@ -87,12 +90,16 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
   const int b = bg / Hkv, g = bg % Hkv;
   // this sequence's counts (capacities with per-sequence lengths)
   int nv, nt, kb;
-  attn_lengths(lens, vis_idx != nullptr, b, n_vis, n_text, k_vis, lane == 0 && split == 0 && g == 0, status,
-               nv, nt, kb);
-  const int T = kb + nt;
+  const bool seq_ok = attn_lengths(lens, vis_idx != nullptr, b, n_vis, n_text, k_vis,
+                                   lane == 0 && split == 0 && g == 0, status, nv, nt, kb);
+  // a fused append adds the new token (cache position nv + nt) as the last one
+  const bool append = APPEND && seq_ok;
+  const int T = kb + nt + (append ? 1 : 0);
   const int t_begin = split * chunk;
   const int t_end = min(T, t_begin + chunk);
   const int32_t* bt = block_table + (size_t)b * max_blocks;
+  if (append && split == 0)
+    store_new_token(k_store, v_store, k_new, v_new, bt, num_blocks, Hkv, D, b, g, nv + nt, lane);
   const int32_t* vrow = vis_idx ? vis_idx + (size_t)bg * k_vis : nullptr;
 
   // Q fragments (A operand, rows = heads of the group, zero beyond G)
@@ -127,10 +134,11 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
       const int tok = j / CPR, c = j % CPR;
       const uint32_t r = __shfl_sync(0xffffffffu, rowid, tok);
       const bool ok = r != kNoRowM;
-      const size_t off = ok ? (size_t)r * D + c * 8 : 0;
+      const bool fresh = APPEND && r == kNewRowId;   // the appended token: from k_new / v_new
+      const size_t off = fresh ? (size_t)bg * D + c * 8 : (ok ? (size_t)r * D + c * 8 : 0);
       const uint32_t dst = (uint32_t)(tok * D * 2 + ((c ^ (tok & 7)) * 16));
-      cp_async16(kbase + dst, k_pool + off, ok ? 16u : 0u);
-      cp_async16(vbase + dst, v_pool + off, ok ? 16u : 0u);
+      cp_async16(kbase + dst, (fresh ? k_new : k_pool) + off, ok ? 16u : 0u);
+      cp_async16(vbase + dst, (fresh ? v_new : v_pool) + off, ok ? 16u : 0u);
     }
     cp_async_commit();
     return rowid;
@@ -186,7 +194,8 @@ sparse_attn_mma_kernel(const uint16_t* __restrict__ q, int H, int G,
       if (p[q4] >= 0) {
         const int page = pg[q4];
         if (page >= 0 && page < num_blocks)
-          rid = (((uint32_t)page * (uint32_t)Hkv + (uint32_t)g) << 4) | (uint32_t)(p[q4] & 15);
+          rid = append && p[q4] == nv + nt ? kNewRowId
+                                           : (((uint32_t)page * (uint32_t)Hkv + (uint32_t)g) << 4) | (uint32_t)(p[q4] & 15);
         else
           flag_status(status, kStatusBadBlock);
       }
@@ -381,14 +390,17 @@ cudaError_t launch_sparse_attn_mma(const AttnArgs& a, const AttnPlan& p, cudaStr
   const unsigned grid = (unsigned)((warps + kMmaWarps - 1) / kMmaWarps);
   const size_t smem = attn_mma_smem_bytes(a.D);
   const int G = a.H / a.Hkv;
-  static bool attr_set[64][2] = {};
+  // the instantiation for this call: head dim and whether it appends a token
+  const bool app = a.k_new != nullptr;
+  auto kernel = a.D == 128 ? (app ? sparse_attn_mma_kernel<128, true> : sparse_attn_mma_kernel<128, false>)
+                           : (app ? sparse_attn_mma_kernel<64, true> : sparse_attn_mma_kernel<64, false>);
+  static bool attr_set[64][4] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int di = a.D == 128 ? 1 : 0;
+  const int di = (a.D == 128 ? 1 : 0) + (app ? 2 : 0);
   if (dev < 0 || dev >= 64 || !attr_set[dev][di]) {
-    e = a.D == 128 ? cudaFuncSetAttribute(sparse_attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                   : cudaFuncSetAttribute(sparse_attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev][di] = true;
   }
@@ -396,11 +408,10 @@ cudaError_t launch_sparse_attn_mma(const AttnArgs& a, const AttnPlan& p, cudaStr
   static_cast<const uint16_t*>(a.q), a.H, G, static_cast<const uint16_t*>(a.k_pool),                        \
       static_cast<const uint16_t*>(a.v_pool), a.num_blocks, a.Hkv, a.block_table, a.max_blocks, a.vis_idx, \
       a.k_vis, a.n_vis, a.n_text, a.scale * kLog2e, a.batch, p.nsplit, p.chunk, a.part_ml, a.part_o,       \
-      a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse, a.lens
-  if (a.D == 128)
-    e = launch_dependent(sparse_attn_mma_kernel<128>, dim3(grid), dim3(kMmaWarps * 32), smem, stream, SV_MMA_ARGS);
-  else
-    e = launch_dependent(sparse_attn_mma_kernel<64>, dim3(grid), dim3(kMmaWarps * 32), smem, stream, SV_MMA_ARGS);
+      a.status, a.split_done, static_cast<uint16_t*>(a.out), a.lse, a.lens,                                \
+      static_cast<const uint16_t*>(a.k_new), static_cast<const uint16_t*>(a.v_new),                         \
+      static_cast<uint16_t*>(const_cast<void*>(a.k_pool)), static_cast<uint16_t*>(const_cast<void*>(a.v_pool))
+  e = launch_dependent(kernel, dim3(grid), dim3(kMmaWarps * 32), smem, stream, SV_MMA_ARGS);
 #undef SV_MMA_ARGS
   return e;
 }

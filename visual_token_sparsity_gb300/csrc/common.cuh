@@ -67,18 +67,45 @@ __device__ __forceinline__ bool seq_lengths(const SeqLens& s, int b, int n_vis, 
 // visual kb (the k_vis listed indices, or all nv visual tokens when there is
 // no index list).  Out-of-range lengths attend nothing; `report` selects the
 // one thread that sets kStatusBadLength.
-__device__ __forceinline__ void attn_lengths(const SeqLens& lens, bool indexed, int b, int n_vis,
+__device__ __forceinline__ bool attn_lengths(const SeqLens& lens, bool indexed, int b, int n_vis,
                                              int n_text, int k_vis, bool report, int* status, int& nv,
                                              int& nt, int& kb) {
   nv = n_vis;
   nt = n_text;
   kb = indexed ? k_vis : n_vis;
-  if (!lens.any()) return;
+  if (!lens.any()) return true;
   SeqLens l = lens;
   if (!indexed) l.k = nullptr;
   const bool ok = seq_lengths(l, b, n_vis, n_text, indexed ? k_vis : 0, nv, nt, kb);
   if (!indexed) kb = nv;
   if (!ok && report) flag_status(status, kStatusBadLength);
+  return ok;
+}
+
+// Row id (page * Hkv + g) * 16 + slot of the cache position `pos` of KV head
+// g, or kNoRowId (kStatusBadBlock) when the page id is outside the pool.
+constexpr uint32_t kNoRowId = 0xffffffffu;
+// The token a fused append-and-attend call appends: read from the caller's
+// k_new / v_new instead of the pool (a pool row id is at most 2^32 - 17).
+constexpr uint32_t kNewRowId = 0xfffffffeu;
+
+// One warp stores the appended token's K and V rows (bf16 [d] each, from
+// k_new / v_new of (sequence b, KV head g)) at cache position pos; a page id
+// outside the pool is reported and skipped, as by the append kernel.
+__device__ __forceinline__ void store_new_token(uint16_t* k_pool, uint16_t* v_pool, const uint16_t* k_new,
+                                                const uint16_t* v_new, const int32_t* bt, int num_blocks,
+                                                int Hkv, int D, int b, int g, int pos, int lane) {
+  const int page = __ldg(bt + (pos >> 4));
+  if (page < 0 || page >= num_blocks) return;   // reported by the attention's row lookup
+  const size_t row = ((size_t)page * Hkv + g) * 16 + (pos & 15);
+  const size_t src = ((size_t)b * Hkv + g) * D;
+  const int cpr = D / 8;                          // 16-byte words per row
+  for (int v = lane; v < 2 * cpr; v += 32) {
+    const bool is_k = v < cpr;
+    const int c = is_k ? v : v - cpr;
+    const uint4 x = *reinterpret_cast<const uint4*>((is_k ? k_new : v_new) + src + c * 8);
+    *reinterpret_cast<uint4*>((is_k ? k_pool : v_pool) + row * D + c * 8) = x;
+  }
 }
 
 // Two bf16 values packed in a 32-bit word -> fp32 (exact).

@@ -90,6 +90,11 @@ struct AttnArgs {
   float* part_o;
   int* split_done;   // zeroed int per (sequence, KV head); left zeroed after the call
   int* status;
+  // fused append: one new token per (sequence, KV head), bf16 [batch][Hkv][D],
+  // stored at text position n_text and attended as the last token (n_text
+  // then counts the tokens before it); nullptr: plain attention
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_sparse_attn_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
