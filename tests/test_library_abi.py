@@ -153,8 +153,9 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
 
 def test_kernel_count_queries(so):
     """Pure host queries: LLaVA-NeXT rows fuse the top-k and the split merge
-    (one kernel each); LongVILA's 50176-key rows need a separate top-k and its
-    12800-token splits a merge kernel."""
+    (one kernel each); LongVILA's 50176-key rows need a separate top-k, and
+    grouped-query attention (G >= 3) always merges its splits in a separate
+    kernel, however short the call."""
     from visual_token_sparsity_gb300 import binding
     lib = binding.load(so)
     assert lib.sv_retrieve_kernel_count(1, 32, 2880) == 1     # a few rows: top-k fused
@@ -163,4 +164,7 @@ def test_kernel_count_queries(so):
     assert lib.sv_retrieve_kernel_count(1, 4, 0) == 0
     assert lib.sv_attn_kernel_count(16, 32, 32, 1440 + 128) == 1
     assert lib.sv_attn_kernel_count(8, 28, 4, 12544 + 256) == 2
+    assert lib.sv_attn_kernel_count(16, 28, 4, 784 + 256) == 2
+    assert lib.sv_attn_kernel_count(1, 28, 4, 40) == 2
+    assert lib.sv_attn_kernel_count(1, 4, 2, 144 + 64) == 1    # the round-loop shape (G 2)
     assert lib.sv_attn_kernel_count(1, 28, 5, 100) == 0   # H not a multiple of n_kv_heads
