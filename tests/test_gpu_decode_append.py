@@ -91,6 +91,8 @@ def assert_same(res, pools):
     (28, 4, 128, 3136, 100, 2, 784, True),     # G 7, tensor-core kernel
     (8, 8, 128, 300, 0, 2, 0, False),          # no index list, the new token is the first text token
     (16, 2, 64, 200, 24, 3, 1, True),          # G 8, one visual token, the new token opens a page
+    (8, 8, 64, 500, 10, 1, 100, True),         # 8 units: 32-token steps, G 1, d 64
+    (16, 8, 128, 900, 33, 1, 300, True),       # 8 units: 32-token steps, G 2, d 128
 ])
 def test_fused_append_matches_two_calls(lib, H, Hkv, d, n_vis, n_text, B, k, indexed):
     shape, bt, q, k_new, v_new, pools = setup(H, Hkv, d, n_vis, n_text, B, k, seed=H + n_vis + B)
