@@ -91,6 +91,7 @@ def assert_same(res, pools):
     (28, 4, 128, 3136, 100, 2, 784, True),     # G 7, tensor-core kernel
     (8, 8, 128, 300, 0, 2, 0, False),          # no index list, the new token is the first text token
     (16, 2, 64, 200, 24, 3, 1, True),          # G 8, one visual token, the new token opens a page
+    (28, 4, 128, 600, 40, 2, 0, False),        # G 7 without an index list (dense over the cache)
     (8, 8, 64, 500, 10, 1, 100, True),         # 8 units: 32-token steps, G 1, d 64
     (16, 8, 128, 900, 33, 1, 300, True),       # 8 units: 32-token steps, G 2, d 128
 ])
@@ -146,3 +147,36 @@ def test_fused_append_matches_the_oracle(lib):
     o_ref, _ = oracle.sparse_decode_attention(q.double().cpu().numpy(), Kl.numpy(), Vl.numpy(), vis.cpu().numpy(),
                                               576, 33)
     assert_attention_close(out.cpu(), o_ref)
+
+
+def test_fused_append_replays_in_a_cuda_graph(lib):
+    """Captured once and replayed, the fused step gives the eager call's bits
+    (no host-side state between calls)."""
+    from visual_token_sparsity_gb300 import binding as sv
+    shape, bt, q, k_new, v_new, pools = setup(4, 2, 64, 576, 32, 1, 144, seed=41)
+    vis = vis_rows(1, 2, 576, 144, seed=42)
+    B, H, Hkv, d = 1, 4, 2, 64
+    n_tok = 144 + 32 + 1
+    outs = []
+    for path, (kp, vp) in enumerate(pools):
+        layer = sv.KvLayer(kp, vp)
+        seqs = sv.SeqBatch(bt, 576, 32)
+        out = torch.zeros(B, H, d, dtype=torch.bfloat16, device=DEV)
+        ws = sv.workspace(sv.sv_attn_workspace_bytes(B, H, Hkv, d, n_tok))
+        call = lambda: sv.sv_decode_append_attn(q, 1 / math.sqrt(d), layer, seqs, k_new, v_new, vis, 144, out,
+                                                None, ws)
+        if path == 0:
+            call()
+        else:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                call()
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize()
+        assert sv.sv_read_device_status(ws) == 0
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(pools[0][0], pools[1][0]) and torch.equal(pools[0][1], pools[1][1])
