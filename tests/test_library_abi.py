@@ -87,6 +87,15 @@ def test_host_validation_rejects_before_launch(so):
     layer1 = binding.sv_kv_layer(_fake(), _fake(), 100, 1, 64)
     assert lib.sv_sparse_decode_attn(_fake(), 17, 0.1, ctypes.byref(layer1), ctypes.byref(seqs), None, 0,
                                      _fake(), None, _fake(), 1 << 20, s) == 2
+    # fused decode step: missing or misaligned new-token rows, no page for the new token
+    fused = lambda seq, kn, vn: lib.sv_decode_append_attn(_fake(), 4, 0.1, ctypes.byref(layer), ctypes.byref(seq),
+                                                          kn, vn, None, 0, _fake(), None, _fake(), 1 << 20, s)
+    assert fused(seqs, None, _fake()) == 1
+    assert b"k_new" in lib.sv_last_error()
+    assert fused(seqs, _fake(0x10008), _fake()) == 1
+    seqs_full = binding.sv_seq_batch(_fake(), 1, 10, 150, 10)    # 160 tokens fill the 10 pages
+    assert fused(seqs_full, _fake(), _fake()) == 1
+    assert b"overflows" in lib.sv_last_error()
     # eviction span outside the text
     assert lib.sv_evict_qa_tokens(ctypes.byref(layer), 1, ctypes.byref(seqs), 5, 11, None, _fake(), 256, s) == 1
     assert seqs.n_text == 10
